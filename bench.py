@@ -1,0 +1,670 @@
+"""Benchmark: batch-one N:M bitmask SpMV on one decode step of a 70B-shaped model.
+
+One *step* is one token through an 80-layer Llama-3.3-70B-shaped decoder: per
+layer four SpMVs (W_qkv 10240x8192, W_o 8192x8192, W_gate+up 57344x8192,
+W_down 8192x28672), 320 nm_spmv calls in all.  The packed weights sit in a
+rotating set of physical layer slots (far larger than the 129 MB L2) that the
+80 logical layers cycle through, so every call streams its weights from HBM.
+
+Reported (one JSON line on stdout, rank 0):
+  value        achieved HBM GB/s of the whole step: algorithmic bytes
+               (values + masks + x + y) / device time, inputs resident;
+  us_per_call  per matrix, from CUDA events around each launch;
+  speedup_vs_dense   dense_gemv step time / nm_spmv step time, same shapes;
+  patterns     the same step for 2:4, 4:8, 8:16, 16:32;
+  e2e          the same metric through the Python/C-ABI calls with x copied
+               in from pinned host memory and y copied back every step;
+  roofline     the SpMV kernel's achieved GB/s over the measured HBM peak;
+  cpu_baseline the plain C oracle on a bounded sample of the same workload.
+Timing: CUDA graph replays timed with CUDA events on the launching stream,
+W untimed warm-up steps, then exactly K timed steps between barriers and
+device synchronisation; L2 is defeated by the rotating set (stated in config).
+
+``--impl reference`` times the CPU oracle instead (the slow reference arm).
+Multi-GPU (torchrun, N ranks): every rank runs an independent replica (the
+path has no exchange step); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "N:M SpMV µs/call & achieved HBM GB/s (% peak) at batch 1; speedup vs dense GEMV"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+
+WORKLOADS = {
+    "llama33_70b_layer": [("qkv", 10240, 8192), ("o", 8192, 8192), ("gate_up", 57344, 8192),
+                          ("down", 8192, 28672)],
+    "qwen3_32b_layer": [("qkv", 10240, 5120), ("o", 5120, 8192), ("gate_up", 51200, 5120),
+                        ("down", 5120, 25600)],
+    "llama31_8b_layer": [("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096),
+                         ("down", 4096, 14336)],
+    "pattern_sweep": [("up", 14336, 4096), ("down", 4096, 14336)],
+    "single_4096": [("W", 4096, 4096)],
+}
+PATTERNS = [(2, 4), (4, 8), (8, 16), (16, 32)]
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (the algorithmic traffic of one call)
+# ---------------------------------------------------------------------------
+def sparse_bytes(rows: int, cols: int) -> int:
+    return rows * cols + rows * cols // 8 + 2 * cols + 2 * rows
+
+
+def dense_bytes(rows: int, cols: int) -> int:
+    return 2 * rows * cols + 2 * cols + 2 * rows
+
+
+# ---------------------------------------------------------------------------
+# multi-rank plumbing (host logic; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_units: float, local_seconds: float, group=None):
+    """Whole-job totals across ranks: (sum of units, max of seconds)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_units, local_seconds
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=dev)
+    s = torch.tensor([float(local_seconds)], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(u.item()), float(s.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = self.smi_id(device_index)
+        self.proc = None
+        self.path = None
+        self.window = [None, None]
+
+    def start(self):
+        import datetime
+        self.window[0] = datetime.datetime.now()
+
+    def stop(self):
+        import datetime
+        self.window[1] = datetime.datetime.now()
+
+    @staticmethod
+    def smi_id(local: int) -> str:
+        """nvidia-smi id of the CUDA device (PCI bus id when torch exposes it)."""
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(local)
+            return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except (AttributeError, RuntimeError):
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [t for t in vis.split(",") if t.strip()]
+            return ids[local].strip() if local < len(ids) else str(local)
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        """Clock samples taken between start() and stop() (all if unmarked)."""
+        import datetime
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9], ts))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        t0, t1 = self.window
+        if t0 is not None and t1 is not None:
+            inside = [r for r in rows if t0 <= r[4] <= t1]
+            rows = inside or rows
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# peaks, profiles
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("spmv.cu", "device.cuh", "split.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "sparse_spmv_memory_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(shape_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    p = os.path.join(ROOT, "profiles", "nm_spmv_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    e = d.get("per_launch", {}).get(shape_key)
+    return None if e is None else float(e["dram_bytes"])
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_pack_sample(mats, pattern, rows_per):
+    """Oracle-packed first ``rows_per`` rows of every matrix (not timed)."""
+    import oracle
+    import synth
+    orc = oracle.Oracle()
+    N, M = pattern
+    packed = []
+    for mi, (name, rows, cols) in enumerate(mats):
+        n = min(rows_per, rows)
+        W = synth.normal_f16((n, cols), 0, synth.stream_id(2, mi, 0), synth.WEIGHT_SIGMA)
+        x = synth.activations(cols, 0, synth.stream_id(2, mi, 1))
+        v, m = orc.prune_pack(W, N, M)
+        packed.append((v, m, cols, x, n))
+    return orc, packed
+
+
+def oracle_run(orc, packed):
+    """The timed oracle work: unpack to dense + double matvec; returns bytes."""
+    nbytes = 0
+    for v, m, cols, x, n in packed:
+        orc.spmv_f64(v, m, cols, x)
+        nbytes += sparse_bytes(n, cols)
+    return nbytes
+
+
+def oracle_sample(mats, pattern, seconds: float):
+    """Grow a sample of rows until the oracle takes about ``seconds`` on it.
+    Returns (rows_per_matrix, bytes, elapsed_s, description)."""
+    rows_per = 8
+    while True:
+        orc, packed = oracle_pack_sample(mats, pattern, rows_per)
+        t0 = time.perf_counter()
+        nbytes = oracle_run(orc, packed)
+        dt = time.perf_counter() - t0
+        full = all(rows_per >= r for _, r, _ in mats)
+        if dt >= seconds * 0.5 or full:
+            desc = (f"first {rows_per} rows of each of the {len(mats)} matrices, "
+                    f"{pattern[0]}:{pattern[1]}, oracle unpack + double matvec, 1 thread")
+            return rows_per, nbytes, dt, desc
+        rows_per = int(rows_per * max(2.0, min(16.0, seconds / max(dt, 1e-4))))
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def make_dense(mats, device):
+    import torch
+    import synth
+    dense, xs = [], []
+    for mi, (name, rows, cols) in enumerate(mats):
+        host = torch.empty((rows, cols), dtype=torch.int16, pin_memory=True)
+        synth.normal_f16_into(host.data_ptr(), rows * cols, 0, synth.stream_id(2, mi, 0),
+                              synth.WEIGHT_SIGMA)
+        dense.append(host.to(device, non_blocking=True).view(torch.float16))
+        xh = synth.activations(cols, 0, synth.stream_id(2, mi, 1))
+        xs.append(torch.from_numpy(xh.view(np.int16)).to(device).view(torch.float16))
+    torch.cuda.synchronize()
+    return dense, xs
+
+
+def pack_slots(nm, dense, pattern, slots):
+    """Pack every matrix once, then copy it into ``slots`` physical layer slots."""
+    import torch
+    N, M = pattern
+    out = []
+    base = [nm.nm_pack(W, N, M) for W in dense]
+    for s in range(slots):
+        if s == 0:
+            out.append(base)
+        else:
+            out.append([(v.clone(), m.clone()) for v, m in base])
+    torch.cuda.synchronize()
+    return out
+
+
+def dense_slots(dense, slots):
+    import torch
+    out = [dense] + [[W.clone() for W in dense] for _ in range(slots - 1)]
+    torch.cuda.synchronize()
+    return out
+
+
+class Step:
+    """The calls of one decode step over `layers` logical layers."""
+
+    def __init__(self, nm, mats, layers, device):
+        import torch
+        self.nm, self.mats, self.layers = nm, mats, layers
+        self.x_off, self.y_off = [], []
+        xo = yo = 0
+        for _, rows, cols in mats:
+            self.x_off.append(xo)
+            self.y_off.append(yo)
+            xo += cols
+            yo += rows
+        self.x_per_layer, self.y_per_layer = xo, yo
+        # per-layer inputs and outputs, contiguous so one copy moves a whole step
+        self.x_all = torch.empty((layers, xo), dtype=torch.float16, device=device)
+        self.y_all = torch.empty((layers, yo), dtype=torch.float16, device=device)
+
+    def fill_x(self, xs):
+        for i, x in enumerate(xs):
+            self.x_all[:, self.x_off[i]:self.x_off[i] + x.numel()] = x
+
+    def x(self, layer, i):
+        _, rows, cols = self.mats[i]
+        return self.x_all[layer, self.x_off[i]:self.x_off[i] + cols]
+
+    def y(self, layer, i):
+        _, rows, cols = self.mats[i]
+        return self.y_all[layer, self.y_off[i]:self.y_off[i] + rows]
+
+    def run_sparse(self, slots, on_launch=None):
+        nm = self.nm
+        for l in range(self.layers):
+            slot = slots[l % len(slots)]
+            for i, (v, m) in enumerate(slot):
+                if on_launch:
+                    on_launch(i, 0)
+                nm.nm_spmv(v, m, self.x(l, i), y=self.y(l, i))
+                if on_launch:
+                    on_launch(i, 1)
+
+    def run_dense(self, slots):
+        nm = self.nm
+        for l in range(self.layers):
+            slot = slots[l % len(slots)]
+            for i, W in enumerate(slot):
+                nm.dense_gemv(W, self.x(l, i), y=self.y(l, i))
+
+    def bytes_sparse(self):
+        return self.layers * sum(sparse_bytes(r, c) for _, r, c in self.mats)
+
+    def bytes_dense(self):
+        return self.layers * sum(dense_bytes(r, c) for _, r, c in self.mats)
+
+    def calls(self):
+        return self.layers * len(self.mats)
+
+
+def time_graph(fn, steps, warmup, stream, clock=None):
+    """Capture fn() in a CUDA graph, replay `warmup` times, then time `steps`
+    replays with CUDA events on `stream`.  Returns per-step ms and total s."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()  # eager once: plan caches and function attributes before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    if clock:
+        clock.start()
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for k in range(steps):
+            g.replay()
+            ev[k + 1].record(stream)
+    torch.cuda.synchronize()
+    if clock:
+        clock.stop()
+    barrier()
+    per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+    total = ev[0].elapsed_time(ev[steps]) / 1e3
+    del g
+    return per, total
+
+
+def time_launches(step, slots, stream, steps):
+    """Eager steps with a CUDA event pair around every nm_spmv launch: the
+    kernel's own durations, per matrix."""
+    import torch
+    n = step.calls() * steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    which = []
+    idx = [0]
+
+    def mark(i, edge):
+        evs[idx[0]].record(stream)
+        if edge == 0:
+            which.append(i)
+        idx[0] += 1
+
+    with torch.cuda.stream(stream):
+        step.run_sparse(slots)  # warm
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            step.run_sparse(slots, on_launch=mark)
+    torch.cuda.synchronize()
+    per_mat = {}
+    for k, i in enumerate(which):
+        per_mat.setdefault(i, []).append(evs[2 * k].elapsed_time(evs[2 * k + 1]) * 1e3)
+    return per_mat  # matrix index -> list of us
+
+
+def run_gpu(args):
+    import torch
+    import sparse_spmv_memory_gb300 as nm
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    nm.lib()
+    mats = WORKLOADS[args.workload]
+    layers = args.layers
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = hbm_peak()
+
+    t_setup = time.time()
+    dense, xs = make_dense(mats, device)
+    step = Step(nm, mats, layers, device)
+    step.fill_x(xs)
+    setup_s = time.time() - t_setup
+
+    head = tuple(int(t) for t in args.pattern.split(":"))
+    patterns = [head] + ([p for p in PATTERNS if p != head] if args.patterns else [])
+    results = {}
+    per_launch = None
+    clocks = None
+    for pat in patterns:
+        slots = pack_slots(nm, dense, pat, args.slots)
+        fn = lambda: step.run_sparse(slots)
+        if pat == head:
+            with ClockSampler(local) as cs:
+                per, total = time_graph(fn, args.steps, args.warmup, stream, clock=cs)
+            clocks = cs.summary()
+            per_launch = time_launches(step, slots, stream, min(args.steps, 3))
+        else:
+            per, total = time_graph(fn, max(3, args.steps // 4), max(3, args.warmup), stream)
+        results[pat] = (per, total, len(per))
+        del slots, fn
+        torch.cuda.empty_cache()
+
+    # end to end through the public calls: pinned host x in, y out, every step
+    slots = pack_slots(nm, dense, head, args.slots)
+    x_host = torch.empty(step.x_all.shape, dtype=torch.float16, pin_memory=True)
+    x_host.copy_(step.x_all)
+    y_host = torch.empty(step.y_all.shape, dtype=torch.float16, pin_memory=True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.x_all.copy_(x_host, non_blocking=True)
+            step.run_sparse(slots)
+            y_host.copy_(step.y_all, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step.x_all.copy_(x_host, non_blocking=True)
+            step.run_sparse(slots)
+            y_host.copy_(step.y_all, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_wall = time.perf_counter() - t0
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    barrier()
+    del slots
+    torch.cuda.empty_cache()
+
+    # dense baseline on the same shapes and rotation scheme
+    dense_res = None
+    if args.dense:
+        dslots = dense_slots(dense, args.dense_slots)
+        dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
+                                  args.warmup, stream)
+        dense_res = (dper, dtotal, len(dper))
+        del dslots
+        torch.cuda.empty_cache()
+
+    # ---- assemble ------------------------------------------------------------
+    per, total, k = results[head]
+    step_bytes = step.bytes_sparse()
+    units, secs = aggregate(step_bytes * k, total)
+    gbs = units / secs / 1e9
+    med_ms = statistics.median(per)
+    out = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": k,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs / k * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp16 in/out, fp32 accumulate",
+        "data": "synthetic (seeded N(0,0.02) fp16 weights, top-N |w| per M-group; N(0,1) fp16 x)",
+        "config": {
+            "workload": (f"{args.workload} x{layers} layers, batch 1, "
+                         + ", ".join(f"{n} {r}x{c}" for n, r, c in mats)),
+            "pattern": f"{head[0]}:{head[1]}",
+            "calls_per_step": step.calls(),
+            "physical_slots": args.slots,
+            "l2_defeat": (f"rotating set of {args.slots} packed layer slots = "
+                          f"{args.slots * step_bytes / layers / 1e9:.1f} GB > L2 (129 MB)"),
+            "parallelism": f"replicas x{world}",
+        },
+        "step_ms": {"median": round(med_ms, 4), "p10": round(float(np.percentile(per, 10)), 4),
+                    "p90": round(float(np.percentile(per, 90)), 4)},
+        "pct_peak": {"of_measured" if peak_kind == "measured" else "of_fallback":
+                     round(gbs / world / peak, 4), "of_nominal_7900": round(gbs / world / NOMINAL_HBM_GBS, 4)},
+        "gpu_launches": step.calls() * k,
+    }
+    # per-matrix kernel durations
+    calls = {}
+    tot_b = tot_us = 0.0
+    for i, (name, rows, cols) in enumerate(mats):
+        us = per_launch.get(i, [])
+        if not us:
+            continue
+        mu = statistics.median(us)
+        calls[name] = {"shape": f"{rows}x{cols}", "us_per_call": round(mu, 2),
+                       "GB_s": round(sparse_bytes(rows, cols) / mu / 1e3, 1),
+                       "bytes": sparse_bytes(rows, cols)}
+        tot_b += sparse_bytes(rows, cols) * len(us)
+        tot_us += sum(us)
+    out["us_per_call"] = calls
+    achieved = tot_b / tot_us / 1e3 if tot_us else None
+    dom = max(mats, key=lambda m: sparse_bytes(m[1], m[2]))
+    traffic = ncu_traffic(f"{dom[1]}x{dom[2]}")
+    out["roofline"] = {
+        "bound": "hbm", "kernel": "nm_spmv (spmv_kernel)",
+        "achieved": None if achieved is None else round(achieved, 1),
+        "peak": peak, "unit": "GB/s",
+        "frac": None if achieved is None else round(achieved / peak, 4),
+        "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+        "traffic": traffic,
+        "traffic_shape": f"{dom[1]}x{dom[2]}",
+        "traffic_algorithmic": sparse_bytes(dom[1], dom[2]),
+        "achieved_basis": "algorithmic bytes of all nm_spmv launches / sum of their CUDA-event durations",
+    }
+    out["patterns"] = {
+        f"{p[0]}:{p[1]}": {"ms_per_step": round(results[p][1] / results[p][2] * 1e3, 4),
+                           "GB_s": round(step_bytes * results[p][2] / results[p][1] / 1e9, 1),
+                           "us_per_call_avg": round(results[p][1] / results[p][2] / step.calls() * 1e6, 2),
+                           "masks_bytes_per_step": layers * sum(r * c // 8 for _, r, c in mats)}
+        for p in patterns}
+    if dense_res:
+        dper, dtotal, dk = dense_res
+        d_ms = dtotal / dk * 1e3
+        out["dense"] = {"ms_per_step": round(d_ms, 4),
+                        "GB_s": round(step.bytes_dense() * dk / dtotal / 1e9, 1),
+                        "physical_slots": args.dense_slots}
+        out["speedup_vs_dense"] = round(d_ms / (total / k * 1e3), 4)
+        out["speedup_ideal"] = round(step.bytes_dense() / step_bytes, 4)
+    xb = step.x_all.numel() * 2
+    yb = step.y_all.numel() * 2
+    e_units, e_secs = aggregate(step_bytes * args.steps, e2e_s)
+    out["e2e"] = {"value": round(e_units / e_secs / 1e9, 1), "unit": "GB/s",
+                  "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
+                  "ms_per_step": round(e_secs / args.steps * 1e3, 4),
+                  "host_wall_ms_per_step": round(e2e_wall / args.steps * 1e3, 4),
+                  "path": "Python binding -> C ABI nm_spmv per call, eager, pinned host x/y"}
+    out["clocks"] = clocks
+    out["setup_s"] = round(setup_s, 1)
+
+    if rank == 0 and world == 1 and args.cpu:
+        _, nb, dt, desc = oracle_sample(mats, head, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    return out
+
+
+def run_reference(args):
+    """The reference arm: the plain CPU oracle, timed as it stands."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    mats = WORKLOADS[args.workload]
+    head = tuple(int(t) for t in args.pattern.split(":"))
+    per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
+    rows_per, _, _, desc = oracle_sample(mats, head, per_step)
+    orc, packed = oracle_pack_sample(mats, head, rows_per)
+    step_bytes = sum(sparse_bytes(n, cols) for _, _, cols, _, n in packed)
+    for _ in range(args.warmup):
+        oracle_run(orc, packed)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_run(orc, packed)
+    secs = time.perf_counter() - t0
+    val = step_bytes * args.steps / secs / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": f"{args.workload}, batch 1, oracle sample", "pattern": args.pattern},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(val, 4),
+                         "unit": "GB/s"},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama33_70b_layer")
+    ap.add_argument("--pattern", default="2:4")
+    ap.add_argument("--layers", type=int, default=80)
+    ap.add_argument("--slots", type=int, default=16, help="physical sparse layer slots")
+    ap.add_argument("--dense-slots", type=int, default=8)
+    ap.add_argument("--no-dense", dest="dense", action="store_false")
+    ap.add_argument("--no-patterns", dest="patterns", action="store_false")
+    ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def main(argv=None):
+    args = parse(argv)
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    out = run_gpu(args) if args.impl == "ours" else run_reference(args)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * nm_spmv.h -- C ABI of the batch-one N:M bitmask SpMV library (sm_103a).
+ *
+ * The operation (SparseDecoding pages):
+ *   - news.bitwarelabs.com summary, "What's new": batch-one LLM decoding is
+ *     memory-bandwidth bound and dominated by sparse matrix-vector products
+ *     y = W x, one per linear layer per generated token.
+ *   - aimodeling.com article, "The Kernel Is the Other Half of the Answer":
+ *     W keeps exactly N of every M weights (2:4, 4:8, 8:16, 16:32, all 50%);
+ *     every 32 input columns of a row are described by one 32-bit mask word
+ *     with exactly 16 set bits, replacing per-nonzero 32-bit column indices,
+ *     and the kernel walks the mask with fixed-step loops.  All four patterns
+ *     carry identical metadata traffic.
+ *   - weekinpapers.com, Abstract: "N:M sparse matrix-vector kernel with
+ *     bitmask indexing and fixed-step traversal".
+ *
+ * Layout of the packed format (readings where the pages are silent):
+ *   W is rows x cols (output dim x input dim), row-major; cols % 32 == 0.
+ *   masks  : uint32 [rows][cols/32]; bit b of word w of row r describes
+ *            column 32*w + b (least significant bit = lowest column).
+ *   values : fp16   [rows][cols/2]; the kept entries of row r in ascending
+ *            column order; row r starts at r*cols/2 and the 16 values of
+ *            mask word w start at r*cols/2 + 16*w (the fixed step).
+ *   An M-group is M consecutive columns starting at a multiple of M, so a
+ *   group never straddles a mask word.  The packed bytes are the same for
+ *   every pattern: rows*cols (values) + rows*cols/8 (masks).
+ *
+ * Conventions for every call:
+ *   - fp16 means IEEE binary16 (CUDA __half); pointers marked "device" must
+ *     point to device (or managed) memory of the current CUDA device.
+ *   - The caller owns every buffer.  Only nm_check_masks allocates (an
+ *     8-byte counter, freed before it returns); the library keeps no
+ *     device memory between calls.  Host state is limited to per-device
+ *     attribute caches.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return at once, except where stated.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns a nonzero nm_status and launches nothing.  A launch
+ *     failure returns NM_ERR_CUDA (the CUDA error is left readable through
+ *     cudaGetLastError's sticky state only if the context itself failed).
+ *   - Calls are thread-safe; concurrent calls on different streams are fine
+ *     as long as their output buffers do not overlap.
+ */
+#ifndef NM_SPMV_H
+#define NM_SPMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NM_OK = 0,
+    NM_ERR_NULL = 1,      /* a required pointer is NULL                        */
+    NM_ERR_SHAPE = 2,     /* rows < 0, cols % 32 != 0, ld < cols, too large    */
+    NM_ERR_PATTERN = 3,   /* (N, M) not one of 2:4, 4:8, 8:16, 16:32           */
+    NM_ERR_ALIGN = 4,     /* a pointer or leading dimension is misaligned      */
+    NM_ERR_WORKSPACE = 5, /* workspace missing or smaller than required        */
+    NM_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed       */
+    NM_ERR_ALIAS = 7      /* an output buffer overlaps an input buffer         */
+} nm_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nm_status_string(int status);
+
+/* Bytes of the packed arrays for a rows x cols matrix; identical for all
+ * four patterns (aimodeling.com, "The Kernel Is the Other Half of the
+ * Answer": identical metadata traffic).  0 for invalid shapes. */
+size_t nm_values_bytes(int64_t rows, int64_t cols); /* rows*cols/2 fp16 = rows*cols bytes */
+size_t nm_masks_bytes(int64_t rows, int64_t cols);  /* rows*cols/32 uint32 = rows*cols/8 bytes */
+
+/* Device workspace nm_spmv needs for this shape, in bytes.  The current
+ * launch plan reduces every row inside one thread block, so this is 0 for
+ * every supported shape; callers may still pass a workspace. */
+size_t nm_spmv_workspace_bytes(int64_t rows, int64_t cols);
+
+/* Largest cols nm_spmv accepts on the current device (the dense x vector is
+ * staged once per thread block in shared memory as fp32). */
+int64_t nm_spmv_max_cols(void);
+
+/* ---------------------------------------------------------------------------
+ * nm_pack -- prune a dense fp16 matrix to N:M and pack it.
+ *   W      : device fp16 [rows][ld], ld >= cols, row stride ld elements.
+ *   N, M   : one of (2,4), (4,8), (8,16), (16,32).
+ *   values : device fp16 [rows][cols/2] (output), 16-byte aligned.
+ *   masks  : device uint32 [rows][cols/32] (output), 4-byte aligned.
+ * Per M-group the N entries with the largest magnitude key
+ * (fp16 bits & 0x7FFF, compared as unsigned; NaN ranks above inf) are kept,
+ * ties going to the lower column.  Integer-only, so the result is bit-exact.
+ * An input that is already N:M-sparse keeps its nonzeros (a kept zero may be
+ * exchanged for a lower-column zero, which leaves the values unchanged).
+ * Outputs must not overlap W.  rows == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int nm_pack(const void *W, int64_t rows, int64_t cols, int64_t ld, int N, int M,
+            void *values, uint32_t *masks, void *stream);
+
+/* nm_unpack -- inverse of nm_pack: scatter values by masks into dense fp16
+ * W_out [rows][ld] (device); unselected columns are written +0.0, columns
+ * >= cols of each row are not touched.  Every mask word must have popcount
+ * 16; a word that does not is decoded in bounds but its row is unspecified. */
+int nm_unpack(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+              void *W_out, int64_t ld, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * nm_spmv -- y = W x for one token (batch 1), W in the packed format.
+ *   values    : device fp16 [rows][cols/2], 32-byte aligned.
+ *   masks     : device uint32 [rows][cols/32], 4-byte aligned.
+ *   x         : device fp16 [cols], 16-byte aligned.
+ *   y         : device fp16 [rows] (output), must not overlap the inputs.
+ *   workspace : device scratch of at least nm_spmv_workspace_bytes(rows,
+ *               cols) bytes (may be NULL when that is 0).
+ * Products and sums are fp32 (fp32 fused multiply-add); y is rounded to fp16
+ * with round-to-nearest-even.  The summation order is fixed for a shape and
+ * device, so repeated calls give bit-identical y.  Takes no N or M: the
+ * packed format is the same for all four patterns.
+ * Precondition: every mask word has popcount 16 (nm_pack guarantees it; use
+ * nm_check_masks for untrusted data).  A word that breaks it is still read
+ * in bounds, but the affected rows are unspecified.
+ * cols must be <= nm_spmv_max_cols(); rows == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+int nm_spmv(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+            const void *x, void *y, void *workspace, size_t workspace_bytes,
+            void *stream);
+
+/* ---------------------------------------------------------------------------
+ * dense_gemv -- the dense baseline y = W x on an unpruned fp16 matrix
+ * (aimodeling.com article, "The Kernel Is the Other Half of the Answer":
+ * speedups are stated against dense decoding throughput).
+ *   W : device fp16 [rows][ld], 16-byte aligned, ld % 8 == 0, ld >= cols.
+ *   x : device fp16 [cols], 16-byte aligned;  y : device fp16 [rows].
+ * Same arithmetic and rounding as nm_spmv.  cols <= nm_spmv_max_cols() * 2.
+ * ------------------------------------------------------------------------- */
+int dense_gemv(const void *W, int64_t rows, int64_t cols, int64_t ld,
+               const void *x, void *y, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Launch plans.  nm_spmv and dense_gemv pick a plan from the shape and the
+ * device: a kernel variant (warps per block x 256-bit steps in flight per
+ * warp) and a grid (one persistent block per SM, never more blocks than
+ * rows).  The _ex forms take the plan explicitly -- variant < 0 or grid <= 0
+ * select the default -- for tuning sweeps and for tests that make rows be
+ * cut between warps and blocks at many different places.  The result is
+ * within the same tolerance for every plan; it is bit-identical across calls
+ * with the same plan.  Bad variants return NM_ERR_SHAPE.
+ * ------------------------------------------------------------------------- */
+int nm_spmv_plan(int64_t rows, int64_t cols, int *variant, int *grid, int *warps);
+int nm_spmv_variant_count(void);
+int nm_spmv_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+               const void *x, void *y, void *workspace, size_t workspace_bytes,
+               int variant, int grid, void *stream);
+int dense_gemv_variant_count(void);
+int dense_gemv_ex(const void *W, int64_t rows, int64_t cols, int64_t ld,
+                  const void *x, void *y, int variant, int grid, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * nm_check_masks -- validator for untrusted masks (host-synchronous).
+ * Returns the number of mask words whose popcount is not 16 (0 = valid), or
+ * a negative nm_status on error.  Allocates and frees an 8-byte device
+ * counter on the stream and waits for the stream.
+ * ------------------------------------------------------------------------- */
+int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NM_SPMV_H */

@@ -1,0 +1,238 @@
+"""Batch-one N:M bitmask SpMV for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libnmspmv.so`` (the C ABI in ``include/nm_spmv.h``).
+It only marshals arguments: tensors become device pointers, the current
+PyTorch stream becomes the ``cudaStream_t``, and output tensors are allocated
+with PyTorch when the caller passes none.  Every step of the computation runs
+in the library's CUDA kernels; there is no fallback path.  Importing works
+without a GPU (so the symbol table can be checked), but the library itself
+must exist: build it with ``__graft_entry__.build()`` or
+``python -m sparse_spmv_memory_gb300._build``.
+
+The operation (SparseDecoding, aimodeling.com article, "The Kernel Is the
+Other Half of the Answer"): y = W x for one token, with W kept N:M-sparse
+(2:4, 4:8, 8:16, 16:32) and stored as compact fp16 values plus one 32-bit
+mask word per 32 input columns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "NMError", "lib", "library_path",
+    "nm_status_string", "nm_values_bytes", "nm_masks_bytes", "nm_spmv_workspace_bytes",
+    "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
+    "nm_check_masks", "nm_spmv_variant_count", "dense_gemv_variant_count",
+]
+
+NM_OK = 0
+STATUS_NAMES = {0: "NM_OK", 1: "NM_ERR_NULL", 2: "NM_ERR_SHAPE", 3: "NM_ERR_PATTERN",
+                4: "NM_ERR_ALIGN", 5: "NM_ERR_WORKSPACE", 6: "NM_ERR_CUDA", 7: "NM_ERR_ALIAS"}
+
+
+class NMError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {nm_status_string(status)}")
+
+
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it with __graft_entry__.build() "
+                "(there is no CPU fallback)")
+        _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "nm_status_string": ([I32], ctypes.c_char_p),
+        "nm_values_bytes": ([I64, I64], SZ),
+        "nm_masks_bytes": ([I64, I64], SZ),
+        "nm_spmv_workspace_bytes": ([I64, I64], SZ),
+        "nm_spmv_max_cols": ([], I64),
+        "nm_pack": ([P, I64, I64, I64, I32, I32, P, P, P], I32),
+        "nm_unpack": ([P, P, I64, I64, P, I64, P], I32),
+        "nm_spmv": ([P, P, I64, I64, P, P, P, SZ, P], I32),
+        "nm_spmv_ex": ([P, P, I64, I64, P, P, P, SZ, I32, I32, P], I32),
+        "nm_spmv_plan": ([I64, I64, P, P, P], I32),
+        "nm_spmv_variant_count": ([], I32),
+        "dense_gemv": ([P, I64, I64, I64, P, P, P], I32),
+        "dense_gemv_ex": ([P, I64, I64, I64, P, P, I32, I32, P], I32),
+        "dense_gemv_variant_count": ([], I32),
+        "nm_check_masks": ([P, I64, I64, P], I64),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    return L
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("nm_* calls take CUDA tensors (there is no CPU path)")
+
+
+def _check(status: int, what: str) -> None:
+    if status != NM_OK:
+        raise NMError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one Python function per entry point
+# ---------------------------------------------------------------------------
+def nm_status_string(status: int) -> str:
+    return lib().nm_status_string(int(status)).decode()
+
+
+def nm_values_bytes(rows: int, cols: int) -> int:
+    return lib().nm_values_bytes(rows, cols)
+
+
+def nm_masks_bytes(rows: int, cols: int) -> int:
+    return lib().nm_masks_bytes(rows, cols)
+
+
+def nm_spmv_workspace_bytes(rows: int, cols: int) -> int:
+    return lib().nm_spmv_workspace_bytes(rows, cols)
+
+
+def nm_spmv_max_cols() -> int:
+    return lib().nm_spmv_max_cols()
+
+
+def nm_spmv_variant_count() -> int:
+    return lib().nm_spmv_variant_count()
+
+
+def dense_gemv_variant_count() -> int:
+    return lib().dense_gemv_variant_count()
+
+
+def nm_spmv_plan(rows: int, cols: int) -> tuple[int, int, int]:
+    v, g, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().nm_spmv_plan(rows, cols, ctypes.byref(v), ctypes.byref(g), ctypes.byref(w)),
+           "nm_spmv_plan")
+    return v.value, g.value, w.value
+
+
+def nm_pack(W, N: int, M: int, cols: int | None = None, values=None, masks=None, stream=None):
+    """Prune dense fp16 W [rows][ld] (first ``cols`` columns) to N:M and pack it.
+    Returns (values fp16 [rows][cols/2], masks int32 [rows][cols/32] holding uint32 bits)."""
+    torch = _torch()
+    _need_cuda(W)
+    rows, ld = W.shape
+    cols = ld if cols is None else cols
+    if W.dtype != torch.float16 or W.stride(1) != 1:
+        raise ValueError("W must be fp16 with unit column stride")
+    if values is None:
+        values = torch.empty((rows, cols // 2), dtype=torch.float16, device=W.device)
+    if masks is None:
+        masks = torch.empty((rows, cols // 32), dtype=torch.int32, device=W.device)
+    _need_cuda(values, masks)
+    _check(lib().nm_pack(_ptr(W), rows, cols, W.stride(0), N, M, _ptr(values), _ptr(masks),
+                         _stream(stream)), "nm_pack")
+    return values, masks
+
+
+def nm_unpack(values, masks, cols: int, out=None, stream=None):
+    """Scatter packed values back to dense fp16 [rows][cols] (+0.0 where unselected)."""
+    torch = _torch()
+    _need_cuda(values, masks)
+    rows = masks.shape[0]
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float16, device=values.device)
+    _need_cuda(out)
+    _check(lib().nm_unpack(_ptr(values), _ptr(masks), rows, cols, _ptr(out), out.stride(0),
+                           _stream(stream)), "nm_unpack")
+    return out
+
+
+def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int = -1,
+            grid: int = 0):
+    """y = W x (fp16 out, fp32 accumulation) on the packed format."""
+    torch = _torch()
+    _need_cuda(values, masks, x)
+    rows = masks.shape[0]
+    cols = x.shape[0]
+    if y is None:
+        y = torch.empty((rows,), dtype=torch.float16, device=x.device)
+    _need_cuda(y, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    L = lib()
+    if variant < 0 and grid <= 0:
+        st = L.nm_spmv(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(y), _ptr(workspace),
+                       ws_bytes, _stream(stream))
+    else:
+        st = L.nm_spmv_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(y),
+                          _ptr(workspace), ws_bytes, variant, grid, _stream(stream))
+    _check(st, "nm_spmv")
+    return y
+
+
+def dense_gemv(W, x, y=None, cols: int | None = None, stream=None, variant: int = -1,
+               grid: int = 0):
+    """Dense baseline y = W x on fp16 W [rows][ld]."""
+    torch = _torch()
+    _need_cuda(W, x)
+    rows, ld = W.shape
+    cols = x.shape[0] if cols is None else cols
+    if y is None:
+        y = torch.empty((rows,), dtype=torch.float16, device=x.device)
+    _need_cuda(y)
+    L = lib()
+    if variant < 0 and grid <= 0:
+        st = L.dense_gemv(_ptr(W), rows, cols, W.stride(0), _ptr(x), _ptr(y), _stream(stream))
+    else:
+        st = L.dense_gemv_ex(_ptr(W), rows, cols, W.stride(0), _ptr(x), _ptr(y), variant, grid,
+                             _stream(stream))
+    _check(st, "dense_gemv")
+    return y
+
+
+def nm_check_masks(masks, cols: int, stream=None) -> int:
+    """Number of mask words whose popcount is not 16 (host-synchronous)."""
+    _need_cuda(masks)
+    r = lib().nm_check_masks(_ptr(masks), masks.shape[0], cols, _stream(stream))
+    if r < 0:
+        raise NMError(-r, "nm_check_masks")
+    return r

@@ -1,0 +1,307 @@
+// api.cu -- the extern "C" boundary: argument checks, launch plans, dispatch.
+// Declarations and the contract of every entry point: include/nm_spmv.h.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <atomic>
+
+#include "../../include/nm_spmv.h"
+#include "kernels.h"
+
+namespace nmk {
+
+// ---- per-device attributes, queried once ------------------------------------
+struct DeviceInfo {
+  int sms;
+  int smem_optin;  // bytes of dynamic shared memory a block may opt into
+};
+
+static constexpr int kMaxDevices = 64;
+static DeviceInfo g_info[kMaxDevices];
+static std::atomic<int> g_info_ready[kMaxDevices];
+
+static cudaError_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && g_info_ready[dev].load(std::memory_order_acquire)) {
+    *out = g_info[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo d{};
+  e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    g_info[dev] = d;
+    g_info_ready[dev].store(1, std::memory_order_release);
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+cudaError_t ensure_max_smem(const void* func, int* done_flags, int max_devices) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < max_devices && __atomic_load_n(&done_flags[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  DeviceInfo d;
+  e = device_info(&d);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
+  if (e == cudaSuccess && dev < max_devices) __atomic_store_n(&done_flags[dev], 1, __ATOMIC_RELEASE);
+  return e;
+}
+
+}  // namespace nmk
+
+using namespace nmk;
+
+namespace {
+
+constexpr int64_t kMaxRows = (int64_t)1 << 31;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return na && nb && a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool valid_pattern(int N, int M) {
+  return (N == 2 && M == 4) || (N == 4 && M == 8) || (N == 8 && M == 16) || (N == 16 && M == 32);
+}
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+int spmv_pitch(int64_t words) { return (int)round_up(words, 32); }
+
+int64_t gemv_steps(int64_t cols) { return (cols + 511) / 512; }
+
+int default_spmv_variant() { return 0; }
+int default_gemv_variant() { return 0; }
+
+// Builds the sparse launch plan; returns NM_OK or a status.
+int make_spmv_plan(int64_t rows, int64_t cols, int variant, int grid, SpmvPlan* plan,
+                   SpmvParams* p) {
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  if (variant < 0) variant = default_spmv_variant();
+  if (variant >= spmv_variant_count()) return NM_ERR_SHAPE;
+  const int nw = spmv_variant_warps(variant);
+  const int64_t words = cols / 32;
+  const int pitch = spmv_pitch(words);
+  if (spmv_smem_bytes(pitch, nw) > (size_t)d.smem_optin) return NM_ERR_SHAPE;
+  if (grid <= 0) grid = d.sms;  // one resident block per SM
+  if (grid > rows) grid = (int)rows;
+  plan->variant = variant;
+  plan->grid = grid;
+  plan->warps = nw;
+  p->rows = rows;
+  p->words = (int)words;
+  p->steps = (int)((words + 31) / 32);
+  p->pitch = pitch;
+  return NM_OK;
+}
+
+int make_gemv_plan(int64_t rows, int64_t cols, int variant, int grid, GemvPlan* plan,
+                   GemvParams* p) {
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  if (variant < 0) variant = default_gemv_variant();
+  if (variant >= gemv_variant_count()) return NM_ERR_SHAPE;
+  const int nw = gemv_variant_warps(variant);
+  const int64_t steps = gemv_steps(cols);
+  if (gemv_smem_bytes((int)steps, nw) > (size_t)d.smem_optin) return NM_ERR_SHAPE;
+  if (grid <= 0) grid = d.sms;
+  if (grid > rows) grid = (int)rows;
+  plan->variant = variant;
+  plan->grid = grid;
+  plan->warps = nw;
+  p->rows = rows;
+  p->cols = (int)cols;
+  p->steps = (int)steps;
+  return NM_OK;
+}
+
+int check_spmv_args(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                    const void* x, const void* y) {
+  if (!values || !masks || !x || !y) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(x, 16) || !aligned(y, 2))
+    return NM_ERR_ALIGN;
+  const size_t yb = (size_t)rows * 2;
+  if (overlap(y, yb, values, (size_t)rows * cols) || overlap(y, yb, masks, (size_t)rows * cols / 8) ||
+      overlap(y, yb, x, (size_t)cols * 2))
+    return NM_ERR_ALIAS;
+  return NM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nm_status_string(int status) {
+  switch (status) {
+    case NM_OK: return "NM_OK";
+    case NM_ERR_NULL: return "NM_ERR_NULL: a required pointer is NULL";
+    case NM_ERR_SHAPE: return "NM_ERR_SHAPE: unsupported shape (rows, cols % 32, ld, size limit)";
+    case NM_ERR_PATTERN: return "NM_ERR_PATTERN: N:M must be 2:4, 4:8, 8:16 or 16:32";
+    case NM_ERR_ALIGN: return "NM_ERR_ALIGN: misaligned pointer or leading dimension";
+    case NM_ERR_WORKSPACE: return "NM_ERR_WORKSPACE: workspace missing or too small";
+    case NM_ERR_CUDA: return "NM_ERR_CUDA: a CUDA call or kernel launch failed";
+    case NM_ERR_ALIAS: return "NM_ERR_ALIAS: an output overlaps an input";
+    default: return "unknown nm_status";
+  }
+}
+
+size_t nm_values_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return 0;
+  return (size_t)rows * (size_t)(cols / 2) * 2;
+}
+
+size_t nm_masks_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return 0;
+  return (size_t)rows * (size_t)(cols / 32) * 4;
+}
+
+size_t nm_spmv_workspace_bytes(int64_t rows, int64_t cols) {
+  (void)rows;
+  (void)cols;
+  return 0;
+}
+
+int64_t nm_spmv_max_cols(void) {
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return -NM_ERR_CUDA;
+  const int nw = spmv_variant_warps(default_spmv_variant());
+  // largest multiple-of-32 pitch whose tile fits, times 32 columns per word
+  int64_t pitch = ((int64_t)d.smem_optin / 4 - 2 * nw) / 33;
+  pitch = pitch / 32 * 32;
+  return pitch * 32;
+}
+
+int nm_pack(const void* W, int64_t rows, int64_t cols, int64_t ld, int N, int M, void* values,
+            uint32_t* masks, void* stream) {
+  if (!W || !values || !masks) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (!valid_pattern(N, M)) return NM_ERR_PATTERN;
+  if (!aligned(W, 2) || !aligned(values, 16) || !aligned(masks, 4)) return NM_ERR_ALIGN;
+  const size_t wb = (size_t)((rows - 1) * ld + cols) * 2;
+  if (rows && (overlap(values, (size_t)rows * cols, W, wb) ||
+               overlap(masks, (size_t)rows * cols / 8, W, wb) ||
+               overlap(values, (size_t)rows * cols, masks, (size_t)rows * cols / 8)))
+    return NM_ERR_ALIAS;
+  if (rows == 0) return NM_OK;
+  cudaError_t e = launch_pack(static_cast<const __half*>(W), rows, cols, ld, M,
+                              static_cast<__half*>(values), masks, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_unpack(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, void* W_out,
+              int64_t ld, void* stream) {
+  if (!values || !masks || !W_out) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (!aligned(values, 16) || !aligned(masks, 4) || !aligned(W_out, 2)) return NM_ERR_ALIGN;
+  const size_t wb = (size_t)((rows - 1) * ld + cols) * 2;
+  if (rows && (overlap(W_out, wb, values, (size_t)rows * cols) ||
+               overlap(W_out, wb, masks, (size_t)rows * cols / 8)))
+    return NM_ERR_ALIAS;
+  if (rows == 0) return NM_OK;
+  cudaError_t e = launch_unpack(static_cast<const __half*>(values), masks, rows, cols,
+                                static_cast<__half*>(W_out), ld, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+               const void* x, void* y, void* workspace, size_t workspace_bytes, int variant,
+               int grid, void* stream) {
+  int st = check_spmv_args(values, masks, rows, cols, x, y);
+  if (st != NM_OK) return st;
+  if (workspace_bytes < nm_spmv_workspace_bytes(rows, cols)) return NM_ERR_WORKSPACE;
+  (void)workspace;
+  if (rows == 0) return NM_OK;
+  SpmvPlan plan;
+  SpmvParams p;
+  st = make_spmv_plan(rows, cols, variant, grid, &plan, &p);
+  if (st != NM_OK) return st;
+  p.values = static_cast<const uint32_t*>(values);
+  p.masks = masks;
+  p.x = static_cast<const __half*>(x);
+  p.y = static_cast<__half*>(y);
+  cudaError_t e = launch_spmv(p, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmv(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* x,
+            void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  return nm_spmv_ex(values, masks, rows, cols, x, y, workspace, workspace_bytes, -1, 0, stream);
+}
+
+int nm_spmv_plan(int64_t rows, int64_t cols, int* variant, int* grid, int* warps) {
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return NM_ERR_SHAPE;
+  SpmvPlan plan;
+  SpmvParams p;
+  int st = make_spmv_plan(rows, cols, -1, 0, &plan, &p);
+  if (st != NM_OK) return st;
+  if (variant) *variant = plan.variant;
+  if (grid) *grid = plan.grid;
+  if (warps) *warps = plan.warps;
+  return NM_OK;
+}
+
+int nm_spmv_variant_count(void) { return spmv_variant_count(); }
+
+int dense_gemv_variant_count(void) { return gemv_variant_count(); }
+
+int dense_gemv_ex(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
+                  int variant, int grid, void* stream) {
+  if (!W || !x || !y) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 8 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (!aligned(W, 16) || ld % 8 != 0 || !aligned(x, 16) || !aligned(y, 2)) return NM_ERR_ALIGN;
+  const size_t yb = (size_t)rows * 2;
+  if (rows && (overlap(y, yb, W, (size_t)((rows - 1) * ld + cols) * 2) ||
+               overlap(y, yb, x, (size_t)cols * 2)))
+    return NM_ERR_ALIAS;
+  if (rows == 0) return NM_OK;
+  GemvPlan plan;
+  GemvParams p;
+  int st = make_gemv_plan(rows, cols, variant, grid, &plan, &p);
+  if (st != NM_OK) return st;
+  p.W = static_cast<const __half*>(W);
+  p.x = static_cast<const __half*>(x);
+  p.y = static_cast<__half*>(y);
+  p.ld = ld;
+  cudaError_t e = launch_gemv(p, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int dense_gemv(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
+               void* stream) {
+  return dense_gemv_ex(W, rows, cols, ld, x, y, -1, 0, stream);
+}
+
+int64_t nm_check_masks(const uint32_t* masks, int64_t rows, int64_t cols, void* stream) {
+  if (!masks) return -NM_ERR_NULL;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return -NM_ERR_SHAPE;
+  if (!aligned(masks, 4)) return -NM_ERR_ALIGN;
+  if (rows == 0) return 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* d_count = nullptr;
+  unsigned long long h_count = 0;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&d_count), sizeof(*d_count), s) != cudaSuccess)
+    return -NM_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(d_count, 0, sizeof(*d_count), s);
+  if (e == cudaSuccess) e = launch_check_masks(masks, rows * (cols / 32), d_count, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&h_count, d_count, sizeof(h_count), cudaMemcpyDeviceToHost, s);
+  cudaError_t ef = cudaFreeAsync(d_count, s);
+  if (e == cudaSuccess) e = ef;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? (int64_t)h_count : -NM_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nmk {
+
+// ---- sparse ----------------------------------------------------------------
+struct SpmvParams {
+  const uint32_t* values;  // fp16 pairs, [rows][words*8] uint32
+  const uint32_t* masks;   // [rows][words]
+  const __half* x;         // [words*32]
+  __half* y;               // [rows]
+  int64_t rows;
+  int words;  // cols / 32
+  int steps;  // ceil(words / 32): warp-steps per row
+  int pitch;  // floats per row of the transposed x tile (multiple of 32, >= words)
+};
+
+struct SpmvPlan {
+  int variant;  // kernel template instance (warps per block, steps in flight)
+  int grid;     // blocks
+  int warps;    // warps per block of that variant
+};
+
+int spmv_variant_warps(int variant);
+int spmv_variant_count();
+size_t spmv_smem_bytes(int pitch, int nw);
+cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, cudaStream_t stream);
+
+// ---- dense -----------------------------------------------------------------
+struct GemvParams {
+  const __half* W;  // [rows][ld]
+  const __half* x;  // [cols]
+  __half* y;        // [rows]
+  int64_t rows;
+  int64_t ld;
+  int cols;
+  int steps;  // ceil(cols / 512)
+};
+
+struct GemvPlan {
+  int variant;
+  int grid;
+  int warps;
+};
+
+int gemv_variant_warps(int variant);
+int gemv_variant_count();
+size_t gemv_smem_bytes(int steps, int nw);
+cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+
+// ---- format ----------------------------------------------------------------
+cudaError_t launch_pack(const __half* W, int64_t rows, int64_t cols, int64_t ld, int M,
+                        __half* values, uint32_t* masks, cudaStream_t stream);
+cudaError_t launch_unpack(const __half* values, const uint32_t* masks, int64_t rows,
+                          int64_t cols, __half* W, int64_t ld, cudaStream_t stream);
+cudaError_t launch_check_masks(const uint32_t* masks, int64_t n_words,
+                               unsigned long long* d_count, cudaStream_t stream);
+
+// Sets the dynamic shared memory limit of `func` to the device maximum once
+// per device.
+cudaError_t ensure_max_smem(const void* func, int* done_flags, int max_devices);
+
+}  // namespace nmk

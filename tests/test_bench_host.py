@@ -1,0 +1,92 @@
+"""Host-side logic of the benchmark: byte accounting, the multi-rank
+aggregation (world size 2 over gloo, on CPU) and the reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_byte_accounting():
+    # values + masks + x + y, and the dense counterpart
+    assert bench.sparse_bytes(4096, 4096) == 4096 * 4096 * 9 // 8 + 2 * 4096 * 2
+    assert bench.dense_bytes(4096, 4096) == 2 * 4096 * 4096 + 4 * 4096
+    mats = bench.WORKLOADS["llama33_70b_layer"]
+    sp = sum(bench.sparse_bytes(r, c) for _, r, c in mats)
+    de = sum(bench.dense_bytes(r, c) for _, r, c in mats)
+    assert abs(sp / 1e6 - 962.9) < 0.2 and abs(de / 1e6 - 1711.6) < 0.2
+    assert 1.77 < de / sp < 1.78
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+AGG_CHILD = r"""
+import os, sys, json
+sys.path.insert(0, sys.argv[1])
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo")
+r = dist.get_rank()
+units, secs = bench.aggregate(1000.0 * (r + 1), 0.5 + r)
+bench.barrier()
+print(json.dumps({"rank": r, "units": units, "secs": secs}))
+dist.destroy_process_group()
+"""
+
+
+def test_aggregate_two_ranks_gloo(tmp_path):
+    script = tmp_path / "agg.py"
+    script.write_text(AGG_CHILD)
+    port = _free_port()
+    procs = []
+    for r in range(2):
+        env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(r),
+                   WORLD_SIZE="2", LOCAL_RANK=str(r))
+        procs.append(subprocess.Popen([sys.executable, str(script), ROOT], env=env,
+                                      stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    for d in res:
+        assert d["units"] == 3000.0 and d["secs"] == 1.5  # sum of units, slowest rank
+
+
+def test_reference_arm_prints_one_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "3", "--warmup", "3", "--ref-seconds", "2",
+                          "--workload", "single_4096"],
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="1")
+    out = subprocess.run([sys.executable, "-c",
+                          f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+                          "a = bench.parse(['--impl', 'reference', '--steps', '3', '--warmup', '3']);"
+                          "print(bench.run_reference(a))"],
+                         capture_output=True, text=True, env=env, timeout=120)
+    assert out.returncode == 0 and out.stdout.strip() == "None"
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.parse(["--warmup", "2"])

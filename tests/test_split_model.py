@@ -1,0 +1,98 @@
+"""CPU model of the row/step split used by the matrix-vector kernels.
+
+Mirrors the index arithmetic of csrc/split.cuh (block row ranges, per-warp
+step ranges, which warp finishes which row, and the ordered sum of rows cut
+between warps) and checks, for many shapes and launch sizes, that every
+(row, step) is read exactly once, every row is written exactly once, and
+every load stays inside the packed arrays.  Run before the kernels ever see
+a GPU; the GPU parity tests then check the kernels themselves.
+"""
+import itertools
+
+import pytest
+
+
+def block_rows(rows, G, c):
+    return rows * c // G, rows * (c + 1) // G
+
+
+def warp_range(F, NW, w):
+    return F * w // NW, F * (w + 1) // NW
+
+
+def simulate(rows, T, G, NW):
+    writes = {}
+    reads = {}
+    for c in range(G):
+        r0, r1 = block_rows(rows, G, c)
+        F = (r1 - r0) * T
+        pf, pl = {}, {}
+        for w in range(NW):
+            sb, se = warp_range(F, NW, w)
+            acc = []
+            for s in range(sb, se):
+                row, t = divmod(s, T)
+                reads[(r0 + row, t)] = reads.get((r0 + row, t), 0) + 1
+                acc.append((r0 + row, t))
+                if t == T - 1 or s == se - 1:
+                    beg, end = row * T, row * T + T
+                    if beg >= sb and end <= se:
+                        writes.setdefault(r0 + row, []).append(sorted(acc))
+                    elif row == sb // T:
+                        pf[w] = acc
+                    else:
+                        pl[w] = acc
+                    acc = []
+        # combine_cut_rows
+        for t_ in range(NW):
+            sb, se = warp_range(F, NW, t_)
+            if sb == se:
+                continue
+            rf, rl = sb // T, (se - 1) // T
+            cut = se % T != 0
+            first = rl != rf or sb % T == 0
+            if not (cut and first):
+                continue
+            total = list(pf[t_] if rl == rf else pl[t_])
+            for u in range(t_ + 1, NW):
+                ub, ue = warp_range(F, NW, u)
+                if ub == ue:
+                    continue
+                total += pf[u]
+                if ue >= (rl + 1) * T:
+                    break
+            writes.setdefault(r0 + rl, []).append(sorted(total))
+    return reads, writes
+
+
+SHAPES = [(1, 1), (1, 4), (3, 1), (7, 3), (33, 2), (300, 2), (257, 4), (1000, 5), (4096, 4),
+          (57, 28), (5, 28)]
+LAUNCH = [(1, 16), (2, 16), (7, 8), (152, 16), (152, 24), (3, 24), (1000, 8)]
+
+
+@pytest.mark.parametrize("rows,T", SHAPES)
+def test_every_step_read_once_every_row_written_once(rows, T):
+    for G, NW in LAUNCH:
+        G = min(G, rows)
+        reads, writes = simulate(rows, T, G, NW)
+        assert set(reads) == {(r, t) for r in range(rows) for t in range(T)}
+        assert all(v == 1 for v in reads.values())
+        assert sorted(writes) == list(range(rows)), (rows, T, G, NW)
+        for r, parts in writes.items():
+            assert len(parts) == 1
+            assert parts[0] == [(r, t) for t in range(T)], (rows, T, G, NW, r)
+
+
+@pytest.mark.parametrize("cols", [32, 96, 992, 1024, 1056, 4096, 5120, 14336, 28672])
+def test_lane_words_stay_inside_the_row(cols):
+    words = cols // 32
+    T = (words + 31) // 32
+    pitch = (words + 31) // 32 * 32
+    for t, lane in itertools.product(range(T), range(32)):
+        w = t * 32 + lane
+        if w < words:
+            assert 8 * w + 8 <= 8 * words          # 256-bit value load inside the row
+        assert w < pitch                           # pad-row read inside the x tile
+    # the x tile: pad row + 32 rows of pitch floats; bfind in {-1..31}
+    for b in range(-1, 32):
+        assert 0 <= (1 + b) * pitch + (words - 1) < 33 * pitch
