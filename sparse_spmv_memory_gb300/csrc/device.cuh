@@ -41,6 +41,20 @@ __device__ __forceinline__ uint4 ld_keep_v4(const void* p) {
   return v;
 }
 
+// Fire-and-forget prefetch of a contiguous global range into L2 (the address
+// must be 16-byte aligned and the size a multiple of 16).  It keeps many more
+// bytes in flight than the registers of the consuming loads could.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Mask of the b low bits, (1 << b) - 1; b >= 32 (and ~0u) gives all ones.
+__device__ __forceinline__ uint32_t low_bits(uint32_t b) {
+  uint32_t r;
+  asm("bmsk.clamp.b32 %0, %1, %2;" : "=r"(r) : "r"(0u), "r"(b));
+  return r;
+}
+
 // Index of the most significant set bit, or 0xFFFFFFFF when w == 0.
 __device__ __forceinline__ uint32_t msb_index(uint32_t w) {
   uint32_t b;
@@ -53,6 +67,18 @@ __device__ __forceinline__ uint32_t bit_at(uint32_t b) {
   uint32_t r;
   asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(1u), "r"(b));
   return r;
+}
+
+__device__ __forceinline__ uint32_t bit_reverse(uint32_t w) {
+  uint32_t r;
+  asm("brev.b32 %0, %1;" : "=r"(r) : "r"(w));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t lds_u16(uint32_t saddr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
+  return v;
 }
 
 __device__ __forceinline__ float lds_f32(uint32_t saddr) {

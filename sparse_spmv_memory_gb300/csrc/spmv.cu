@@ -16,15 +16,24 @@
 //    32*t + l, reads its 16 values with one 256-bit load and its mask with one
 //    32-bit load.  A warp's step is 1 KiB of values + 128 B of masks, fully
 //    contiguous.  U steps are in flight per warp, double-buffered in registers.
+//  * Two kernels share the decode: spmv_full_kernel for rows whose mask words
+//    fill whole steps (cols % 1024 == 0, every decode-layer shape), where a
+//    warp's steps are one contiguous stretch of memory walked by pointer
+//    increments with no per-lane predication; spmv_kernel for any other cols
+//    (ragged last step, lanes past the row end load nothing).
 //  * x is staged once per block in shared memory as fp32, TRANSPOSED:
 //    xs[b][w] = x[32*w + b].  Lanes of a warp always work on 32 consecutive
 //    words, so whatever bit b each lane is at, the 32 reads fall in 32
 //    distinct banks: the gather never has a bank conflict, for any pattern.
-//    A zero pad row sits at b = -1; bfind() of an exhausted (or corrupt) mask
-//    returns -1, so every read stays inside the array without a branch.
-//  * Decode: most-significant set bit first (bfind), so nonzero k = 15..0 is
-//    matched with value k; fp32 FMA into two accumulators; warp butterfly;
-//    rows cut between warps are summed in warp order (deterministic).
+//  * Decode: the 16 trips of a word run as two independent chains of 8 -- the
+//    upper values 15..8 scan the mask from its most significant bit (bfind),
+//    the lower values 0..7 scan the bit-reversed mask the same way (so from the
+//    least significant bit) -- which halves the serial bit-scan latency.  Zero
+//    pad rows sit at b = -1 and b = 32 of the x tile; an exhausted (or
+//    corrupt) mask makes bfind return -1, which lands in a pad row, so every
+//    read stays inside the tile without a branch.  fp32 FMA (or, with x kept as
+//    fp16, one mixed fp16*fp16+fp32 FMA), warp butterfly, and rows cut between
+//    warps summed in warp order (deterministic).
 //  * No tensor cores: batch-one SpMV does ~0.9 flop per byte, far below the
 //    tensor roofline; the bound is HBM bandwidth.
 #include <cuda_fp16.h>
@@ -43,6 +52,91 @@ struct SpmvBatch {
   uint32_t v[U][8];
 };
 
+// x tile layout in shared memory: rows of P 32-bit slots; row 0 and row 33 are
+// zero pad rows, row 1 + b holds column b of every mask word.  DEC 1 keeps x as
+// fp32, DEC 2/3 keep its fp16 bits in the low half of each slot.
+template <int DEC>
+__device__ __forceinline__ void stage_x(float* xs, const __half* x, int words, int P, int nthreads) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < P; i += nthreads) {
+    xs[i] = 0.f;
+    xs[33 * P + i] = 0.f;
+  }
+  for (int c = warp; c * 32 < words; c += nthreads / 32) {
+    const int w = c * 32 + lane;
+    if (w < words) {
+      const uint4* src = reinterpret_cast<const uint4*>(x) + (int64_t)w * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 h = ld_keep_v4(src + q);
+        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int b = q * 8 + j * 2;
+          if (DEC == 1) {
+            const float2 f = half2_bits_to_float2(hw[j]);
+            xs[(1 + b) * P + w] = f.x;
+            xs[(2 + b) * P + w] = f.y;
+          } else {
+            reinterpret_cast<uint32_t*>(xs)[(1 + b) * P + w] = hw[j] & 0xFFFFu;
+            reinterpret_cast<uint32_t*>(xs)[(2 + b) * P + w] = hw[j] >> 16;
+          }
+        }
+      }
+    }
+  }
+}
+
+// The fixed-step traversal of one mask word: 16 trips as two independent
+// chains of 8.  The upper chain scans the mask from its most significant bit
+// (bfind gives the column b directly) and pairs it with values 15..8; the
+// lower chain scans the bit-reversed mask the same way (bfind gives 31 - b)
+// and pairs it with values 0..7.  col_addr is the shared address of (b = 0,
+// this word); an exhausted chain gets bfind = ~0u and reads a zero pad row.
+// DEC 1: fp32 x, fp16 -> fp32 convert + fp32 FMA.
+// DEC 2: fp16 x, one mixed fp16*fp16+fp32 FMA; clears the scanned bit by xor.
+// DEC 3: as 2, clearing the scanned bit and all above it with bmsk.
+template <int DEC>
+__device__ __forceinline__ void decode_word(uint32_t m, const uint32_t (&v)[8], uint32_t col_addr,
+                                            uint32_t row_bytes, float& a0, float& a1) {
+  uint32_t mh = m;
+  uint32_t ml = bit_reverse(m);
+  const uint32_t top = col_addr + 31u * row_bytes;
+  const uint32_t neg_row = 0u - row_bytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bh = msb_index(mh);
+    const uint32_t bl = msb_index(ml);
+    const uint32_t ah = col_addr + bh * row_bytes;  // bh = ~0u -> pad row 0
+    const uint32_t al = top + bl * neg_row;         // bl = ~0u -> pad row 33
+    if (DEC == 3) {
+      mh &= low_bits(bh);
+      ml &= low_bits(bl);
+    } else {
+      mh ^= bit_at(bh);
+      ml ^= bit_at(bl);
+    }
+    const int kh = 15 - k, kl = k;
+    if (DEC == 1) {
+      const float xh = lds_f32(ah), xl = lds_f32(al);
+      const float2 wh = half2_bits_to_float2(v[kh >> 1]);
+      const float2 wl = half2_bits_to_float2(v[kl >> 1]);
+      a1 = fmaf((kh & 1) ? wh.y : wh.x, xh, a1);
+      a0 = fmaf((kl & 1) ? wl.y : wl.x, xl, a0);
+    } else {
+      const uint16_t xh = lds_u16(ah), xl = lds_u16(al);
+      const uint16_t wh = (kh & 1) ? (uint16_t)(v[kh >> 1] >> 16) : (uint16_t)(v[kh >> 1] & 0xFFFFu);
+      const uint16_t wl = (kl & 1) ? (uint16_t)(v[kl >> 1] >> 16) : (uint16_t)(v[kl >> 1] & 0xFFFFu);
+      a1 = fma_f16f16_f32(wh, xh, a1);
+      a0 = fma_f16f16_f32(wl, xl, a0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// General kernel: any cols (cols % 32 == 0).  Lanes whose word lies past the
+// row end, and steps past the warp's range, load nothing (mask 0, values 0).
+// ---------------------------------------------------------------------------
 struct SpmvCursor {
   int64_t s;    // next flattened step
   int64_t row;  // its local row
@@ -69,7 +163,7 @@ __device__ __forceinline__ void spmv_load(SpmvBatch<U>& bt, SpmvCursor& c, int64
       bt.m[i] = ld_stream_u32(p.masks + word);
       ld_stream_v8(p.values + word * 8, bt.v[i]);
     } else {
-      bt.m[i] = 0u;  // decodes to the zero pad row
+      bt.m[i] = 0u;  // decodes to the zero pad rows
 #pragma unroll
       for (int j = 0; j < 8; ++j) bt.v[i][j] = 0u;
     }
@@ -77,29 +171,13 @@ __device__ __forceinline__ void spmv_load(SpmvBatch<U>& bt, SpmvCursor& c, int64
   }
 }
 
-// The fixed-step traversal of one mask word: 16 trips, unrolled.
-__device__ __forceinline__ void spmv_word(uint32_t m, const uint32_t (&v)[8], uint32_t col_addr,
-                                          uint32_t row_bytes, float& a0, float& a1) {
-#pragma unroll
-  for (int k = 15; k >= 0; --k) {
-    const uint32_t b = msb_index(m);                 // column within the word, or ~0u
-    const float xv = lds_f32(col_addr + b * row_bytes);
-    m ^= bit_at(b);
-    const float2 w2 = half2_bits_to_float2(v[k >> 1]);
-    if (k & 1)
-      a1 = fmaf(w2.y, xv, a1);
-    else
-      a0 = fmaf(w2.x, xv, a0);
-  }
-}
-
-template <int NW, int U>
+template <int NW, int U, int DEC>
 __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;
-  float* xs = smem;             // [33][P]: pad row, then b = 0..31
-  float* pf = smem + 33 * P;    // [NW] first-row partials
-  float* pl = pf + NW;          // [NW] last-row partials
+  float* xs = smem;           // [34][P]
+  float* pf = smem + 34 * P;  // [NW] first-row partials
+  float* pl = pf + NW;        // [NW] last-row partials
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.steps;
@@ -111,27 +189,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
   SpmvBatch<U> A, B;
   // Start the first weight loads before staging x so both latencies overlap.
   spmv_load<U>(A, lc, wr.se, T, p, br.r0, lane);
-
-  // Stage x transposed: xs[1 + b][w] = x[32 w + b]; row 0 is zero.
-  for (int i = threadIdx.x; i < P; i += NW * 32) xs[i] = 0.f;
-  for (int c = warp; c * 32 < p.words; c += NW) {
-    const int w = c * 32 + lane;
-    if (w < p.words) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.x) + (int64_t)w * 4;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 h = ld_keep_v4(src + q);
-        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = half2_bits_to_float2(hw[j]);
-          const int b = q * 8 + j * 2;
-          xs[(1 + b) * P + w] = f.x;
-          xs[(2 + b) * P + w] = f.y;
-        }
-      }
-    }
-  }
+  stage_x<DEC>(xs, p.x, p.words, P, NW * 32);
   __syncthreads();
 
   const uint32_t xs_base = smem_addr(xs);
@@ -146,7 +204,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
     for (int i = 0; i < U; ++i) {
       if (cc.s < wr.se) {
         const uint32_t col_addr = xs_base + row_bytes + 4u * (uint32_t)(cc.t * 32 + lane);
-        spmv_word(bt.m[i], bt.v[i], col_addr, row_bytes, a0, a1);
+        decode_word<DEC>(bt.m[i], bt.v[i], col_addr, row_bytes, a0, a1);
         if (cc.t == T - 1 || cc.s == wr.se - 1) {
           const float v = warp_sum(a0 + a1);
           finish_row(cc.row, v, wr, T, warp, lane, pf, pl, store);
@@ -170,22 +228,118 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
   combine_cut_rows<NW>(F, T, pf, pl, store);
 }
 
-template <int NW, int U>
-static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, cudaStream_t stream) {
-  static int smem_set[64] = {0};
-  auto* k = spmv_kernel<NW, U>;
-  cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
-  if (e != cudaSuccess) return e;
-  k<<<grid, NW * 32, spmv_smem_bytes(p.pitch, NW), stream>>>(p);
-  return cudaGetLastError();
+// ---------------------------------------------------------------------------
+// Whole-step kernel: cols % 1024 == 0, so every lane of every step has a word
+// and a warp's steps are one contiguous stretch of the values and masks
+// arrays.  Loads walk two pointers; full batches of U steps run without any
+// predication; at most U - 1 trailing steps run one at a time.  A block's
+// step count must fit in int (checked on the host).
+// ---------------------------------------------------------------------------
+template <int U>
+__device__ __forceinline__ void load_steps(SpmvBatch<U>& bt, const uint32_t*& vp,
+                                           const uint32_t*& mp) {
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    bt.m[i] = ld_stream_u32(mp);
+    ld_stream_v8(vp, bt.v[i]);
+    mp += 32;   // 32 mask words per step
+    vp += 256;  // 32 words x 16 fp16 values per step
+  }
+}
+
+template <int NW, int U, int DEC>
+__global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams p) {
+  extern __shared__ __align__(16) float smem[];
+  const int P = p.pitch;  // == words
+  float* xs = smem;
+  float* pf = smem + 34 * P;
+  float* pl = pf + NW;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.steps;
+  const BlockRows br = block_rows(p.rows);
+  const int F = (int)((br.r1 - br.r0) * T);
+  const WarpRange wr = warp_range<NW>(F, warp);
+  const int sb = (int)wr.sb, se = (int)wr.se;
+  const int nfull = (se - sb) / U;
+
+  const int64_t g = br.r0 * T + sb;  // global index of the warp's first step
+  const uint32_t* mp = p.masks + g * 32 + lane;
+  const uint32_t* vp = p.values + (g * 32 + lane) * 8;
+
+  SpmvBatch<U> A, B;
+  if (nfull > 0) load_steps<U>(A, vp, mp);
+  stage_x<DEC>(xs, p.x, p.words, P, NW * 32);
+  __syncthreads();
+
+  const uint32_t row_bytes = 4u * (uint32_t)P;
+  const uint32_t lane_col = smem_addr(xs) + row_bytes + 4u * (uint32_t)lane;
+  auto store = [&](int64_t row, float v) { p.y[br.r0 + row] = __float2half_rn(v); };
+
+  int row = sb / T, t = sb - row * T;
+  uint32_t col_addr = lane_col + 128u * (uint32_t)t;
+  float a0 = 0.f, a1 = 0.f;
+
+  auto step = [&](uint32_t m, const uint32_t (&v)[8]) {
+    decode_word<DEC>(m, v, col_addr, row_bytes, a0, a1);
+    col_addr += 128u;
+    if (++t == T) {  // row complete
+      finish_row(row, warp_sum(a0 + a1), wr, T, warp, lane, pf, pl, store);
+      a0 = 0.f;
+      a1 = 0.f;
+      t = 0;
+      ++row;
+      col_addr = lane_col;
+    }
+  };
+
+  for (int i = 0; i < nfull; i += 2) {
+    if (i + 1 < nfull) load_steps<U>(B, vp, mp);
+#pragma unroll
+    for (int u = 0; u < U; ++u) step(A.m[u], A.v[u]);
+    if (i + 1 >= nfull) break;
+    if (i + 2 < nfull) load_steps<U>(A, vp, mp);
+#pragma unroll
+    for (int u = 0; u < U; ++u) step(B.m[u], B.v[u]);
+  }
+  for (int s = sb + nfull * U; s < se; ++s) {
+    SpmvBatch<1> one;
+    load_steps<1>(one, vp, mp);
+    step(one.m[0], one.v[0]);
+  }
+  if (se > sb && t != 0)  // the warp's range ends inside a row
+    finish_row(row, warp_sum(a0 + a1), wr, T, warp, lane, pf, pl, store);
+
+  __syncthreads();
+  combine_cut_rows<NW>(F, T, pf, pl, store);
 }
 
 size_t spmv_smem_bytes(int pitch, int nw) {
-  return (size_t)(33 * pitch + 2 * nw) * sizeof(float);
+  return (size_t)(34 * pitch + 2 * nw) * sizeof(float);
 }
 
-// (warps per block, steps in flight per warp)
-static const int kSpmvVariants[][2] = {{16, 4}, {24, 2}, {16, 2}, {8, 4}, {8, 8}};
+template <int NW, int U, int DEC>
+static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, cudaStream_t stream) {
+  static int smem_full[64] = {0}, smem_gen[64] = {0};
+  const size_t smem = spmv_smem_bytes(p.pitch, NW);
+  const int64_t block_steps = (p.rows + grid - 1) / grid * p.steps;
+  if (p.words % 32 == 0 && block_steps < (int64_t)0x7FFFFFFF) {
+    auto* k = spmv_full_kernel<NW, U, DEC>;
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_full, 64);
+    if (e != cudaSuccess) return e;
+    k<<<grid, NW * 32, smem, stream>>>(p);
+  } else {
+    auto* k = spmv_kernel<NW, U, DEC>;
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_gen, 64);
+    if (e != cudaSuccess) return e;
+    k<<<grid, NW * 32, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// (warps per block, steps in flight per warp, decode)
+static const int kSpmvVariants[][3] = {{16, 4, 2}, {24, 2, 2}, {24, 2, 3}, {24, 2, 1},
+                                       {32, 1, 2}, {16, 2, 2}, {20, 3, 2}, {20, 2, 2}};
 
 int spmv_variant_count() { return (int)(sizeof(kSpmvVariants) / sizeof(kSpmvVariants[0])); }
 
@@ -195,11 +349,14 @@ int spmv_variant_warps(int variant) {
 
 cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, cudaStream_t stream) {
   switch (plan.variant) {
-    case 0: return launch_spmv_t<16, 4>(p, plan.grid, stream);
-    case 1: return launch_spmv_t<24, 2>(p, plan.grid, stream);
-    case 2: return launch_spmv_t<16, 2>(p, plan.grid, stream);
-    case 3: return launch_spmv_t<8, 4>(p, plan.grid, stream);
-    case 4: return launch_spmv_t<8, 8>(p, plan.grid, stream);
+    case 0: return launch_spmv_t<16, 4, 2>(p, plan.grid, stream);
+    case 1: return launch_spmv_t<24, 2, 2>(p, plan.grid, stream);
+    case 2: return launch_spmv_t<24, 2, 3>(p, plan.grid, stream);
+    case 3: return launch_spmv_t<24, 2, 1>(p, plan.grid, stream);
+    case 4: return launch_spmv_t<32, 1, 2>(p, plan.grid, stream);
+    case 5: return launch_spmv_t<16, 2, 2>(p, plan.grid, stream);
+    case 6: return launch_spmv_t<20, 3, 2>(p, plan.grid, stream);
+    case 7: return launch_spmv_t<20, 2, 2>(p, plan.grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

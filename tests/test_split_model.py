@@ -65,6 +65,59 @@ def simulate(rows, T, G, NW):
     return reads, writes
 
 
+def simulate_whole_step(rows, T, G, NW, U):
+    """The whole-step kernel's control flow: full batches of U steps, then
+    single steps; a row is finished when its last step is done or, cut, when
+    the warp's range ends inside it."""
+    writes, reads = {}, {}
+    for c in range(G):
+        r0, r1 = block_rows(rows, G, c)
+        F = (r1 - r0) * T
+        pf, pl = {}, {}
+        for w in range(NW):
+            sb, se = warp_range(F, NW, w)
+            row, t = divmod(sb, T)
+            acc = []
+            steps = list(range(sb, sb + (se - sb) // U * U)) + list(range(sb + (se - sb) // U * U, se))
+
+            def finish(row, acc):
+                beg, end = row * T, row * T + T
+                if beg >= sb and end <= se:
+                    writes.setdefault(r0 + row, []).append(sorted(acc))
+                elif row == sb // T:
+                    pf[w] = acc
+                else:
+                    pl[w] = acc
+
+            for s in steps:
+                assert (row, t) == divmod(s, T)
+                reads[(r0 + row, t)] = reads.get((r0 + row, t), 0) + 1
+                acc.append((r0 + row, t))
+                t += 1
+                if t == T:
+                    finish(row, acc)
+                    acc, t, row = [], 0, row + 1
+            if se > sb and t != 0:
+                finish(row, acc)
+        for t_ in range(NW):
+            sb, se = warp_range(F, NW, t_)
+            if sb == se:
+                continue
+            rf, rl = sb // T, (se - 1) // T
+            if not (se % T != 0 and (rl != rf or sb % T == 0)):
+                continue
+            total = list(pf[t_] if rl == rf else pl[t_])
+            for u in range(t_ + 1, NW):
+                ub, ue = warp_range(F, NW, u)
+                if ub == ue:
+                    continue
+                total += pf[u]
+                if ue >= (rl + 1) * T:
+                    break
+            writes.setdefault(r0 + rl, []).append(sorted(total))
+    return reads, writes
+
+
 SHAPES = [(1, 1), (1, 4), (3, 1), (7, 3), (33, 2), (300, 2), (257, 4), (1000, 5), (4096, 4),
           (57, 28), (5, 28)]
 LAUNCH = [(1, 16), (2, 16), (7, 8), (152, 16), (152, 24), (3, 24), (1000, 8)]
@@ -83,6 +136,17 @@ def test_every_step_read_once_every_row_written_once(rows, T):
             assert parts[0] == [(r, t) for t in range(T)], (rows, T, G, NW, r)
 
 
+@pytest.mark.parametrize("rows,T", SHAPES)
+def test_whole_step_kernel_control_flow(rows, T):
+    for (G, NW), U in itertools.product(LAUNCH, (1, 2, 3, 4)):
+        G = min(G, rows)
+        reads, writes = simulate_whole_step(rows, T, G, NW, U)
+        assert all(v == 1 for v in reads.values()) and len(reads) == rows * T
+        assert sorted(writes) == list(range(rows))
+        for r, parts in writes.items():
+            assert len(parts) == 1 and parts[0] == [(r, t) for t in range(T)]
+
+
 @pytest.mark.parametrize("cols", [32, 96, 992, 1024, 1056, 4096, 5120, 14336, 28672])
 def test_lane_words_stay_inside_the_row(cols):
     words = cols // 32
@@ -93,6 +157,9 @@ def test_lane_words_stay_inside_the_row(cols):
         if w < words:
             assert 8 * w + 8 <= 8 * words          # 256-bit value load inside the row
         assert w < pitch                           # pad-row read inside the x tile
-    # the x tile: pad row + 32 rows of pitch floats; bfind in {-1..31}
+    # the x tile: pad row, 32 rows of pitch floats, pad row.  The upper chain
+    # reads row 1 + b for bfind b in {-1..31}; the lower chain reads row
+    # 1 + (31 - b) for bfind b of the reversed mask in {-1..31}.
     for b in range(-1, 32):
-        assert 0 <= (1 + b) * pitch + (words - 1) < 33 * pitch
+        for row in (1 + b, 1 + (31 - b)):
+            assert 0 <= row * pitch + (words - 1) < 34 * pitch
