@@ -136,6 +136,21 @@ int dense_gemv(const void *W, int64_t rows, int64_t cols, int64_t ld,
                const void *x, void *y, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Launch flags (the _ex entry points take them; nm_spmv and dense_gemv use
+ * NM_FLAG_PDL).
+ *   NM_FLAG_PDL: launch with programmatic dependent launch, so the kernel can
+ *     be scheduled while the previous kernel on the stream drains.  It waits
+ *     for that kernel's completion before reading or writing any buffer, so
+ *     stream order is kept for every argument.
+ *   NM_FLAG_WEIGHTS_CONST: the caller promises that the weights (values and
+ *     masks, or W) were not written by the previous kernel on the stream; the
+ *     first weight loads are then issued before that wait.  x and y are still
+ *     touched only after it.  Only meaningful with NM_FLAG_PDL.
+ * ------------------------------------------------------------------------- */
+#define NM_FLAG_PDL 1
+#define NM_FLAG_WEIGHTS_CONST 2
+
+/* ---------------------------------------------------------------------------
  * Launch plans.  nm_spmv and dense_gemv pick a plan from the shape and the
  * device: a kernel variant (warps per block x 256-bit steps in flight per
  * warp) and a grid (one persistent block per SM, never more blocks than
@@ -149,10 +164,10 @@ int nm_spmv_plan(int64_t rows, int64_t cols, int *variant, int *grid, int *warps
 int nm_spmv_variant_count(void);
 int nm_spmv_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                const void *x, void *y, void *workspace, size_t workspace_bytes,
-               int variant, int grid, void *stream);
+               int variant, int grid, int flags, void *stream);
 int dense_gemv_variant_count(void);
 int dense_gemv_ex(const void *W, int64_t rows, int64_t cols, int64_t ld,
-                  const void *x, void *y, int variant, int grid, void *stream);
+                  const void *x, void *y, int variant, int grid, int flags, void *stream);
 
 /* ---------------------------------------------------------------------------
  * nm_check_masks -- validator for untrusted masks (host-synchronous).

@@ -29,6 +29,8 @@ __all__ = [
 ]
 
 NM_OK = 0
+NM_FLAG_PDL = 1
+NM_FLAG_WEIGHTS_CONST = 2
 STATUS_NAMES = {0: "NM_OK", 1: "NM_ERR_NULL", 2: "NM_ERR_SHAPE", 3: "NM_ERR_PATTERN",
                 4: "NM_ERR_ALIGN", 5: "NM_ERR_WORKSPACE", 6: "NM_ERR_CUDA", 7: "NM_ERR_ALIAS"}
 
@@ -70,11 +72,11 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_pack": ([P, I64, I64, I64, I32, I32, P, P, P], I32),
         "nm_unpack": ([P, P, I64, I64, P, I64, P], I32),
         "nm_spmv": ([P, P, I64, I64, P, P, P, SZ, P], I32),
-        "nm_spmv_ex": ([P, P, I64, I64, P, P, P, SZ, I32, I32, P], I32),
+        "nm_spmv_ex": ([P, P, I64, I64, P, P, P, SZ, I32, I32, I32, P], I32),
         "nm_spmv_plan": ([I64, I64, P, P, P], I32),
         "nm_spmv_variant_count": ([], I32),
         "dense_gemv": ([P, I64, I64, I64, P, P, P], I32),
-        "dense_gemv_ex": ([P, I64, I64, I64, P, P, I32, I32, P], I32),
+        "dense_gemv_ex": ([P, I64, I64, I64, P, P, I32, I32, I32, P], I32),
         "dense_gemv_variant_count": ([], I32),
         "nm_check_masks": ([P, I64, I64, P], I64),
     }
@@ -188,8 +190,9 @@ def nm_unpack(values, masks, cols: int, out=None, stream=None):
 
 
 def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int = -1,
-            grid: int = 0):
-    """y = W x (fp16 out, fp32 accumulation) on the packed format."""
+            grid: int = 0, flags: int | None = None):
+    """y = W x (fp16 out, fp32 accumulation) on the packed format.  ``variant``,
+    ``grid`` and ``flags`` select nm_spmv_ex (defaults: the library's plan)."""
     torch = _torch()
     _need_cuda(values, masks, x)
     rows = masks.shape[0]
@@ -199,18 +202,19 @@ def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int 
     _need_cuda(y, workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     L = lib()
-    if variant < 0 and grid <= 0:
+    if variant < 0 and grid <= 0 and flags is None:
         st = L.nm_spmv(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(y), _ptr(workspace),
                        ws_bytes, _stream(stream))
     else:
         st = L.nm_spmv_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(y),
-                          _ptr(workspace), ws_bytes, variant, grid, _stream(stream))
+                          _ptr(workspace), ws_bytes, variant, grid,
+                          NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "nm_spmv")
     return y
 
 
 def dense_gemv(W, x, y=None, cols: int | None = None, stream=None, variant: int = -1,
-               grid: int = 0):
+               grid: int = 0, flags: int | None = None):
     """Dense baseline y = W x on fp16 W [rows][ld]."""
     torch = _torch()
     _need_cuda(W, x)
@@ -220,11 +224,11 @@ def dense_gemv(W, x, y=None, cols: int | None = None, stream=None, variant: int 
         y = torch.empty((rows,), dtype=torch.float16, device=x.device)
     _need_cuda(y)
     L = lib()
-    if variant < 0 and grid <= 0:
+    if variant < 0 and grid <= 0 and flags is None:
         st = L.dense_gemv(_ptr(W), rows, cols, W.stride(0), _ptr(x), _ptr(y), _stream(stream))
     else:
         st = L.dense_gemv_ex(_ptr(W), rows, cols, W.stride(0), _ptr(x), _ptr(y), variant, grid,
-                             _stream(stream))
+                             NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "dense_gemv")
     return y
 

@@ -228,7 +228,7 @@ int nm_unpack(const void* values, const uint32_t* masks, int64_t rows, int64_t c
 
 int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                const void* x, void* y, void* workspace, size_t workspace_bytes, int variant,
-               int grid, void* stream) {
+               int grid, int flags, void* stream) {
   int st = check_spmv_args(values, masks, rows, cols, x, y);
   if (st != NM_OK) return st;
   if (workspace_bytes < nm_spmv_workspace_bytes(rows, cols)) return NM_ERR_WORKSPACE;
@@ -242,13 +242,15 @@ int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
   p.masks = masks;
   p.x = static_cast<const __half*>(x);
   p.y = static_cast<__half*>(y);
-  cudaError_t e = launch_spmv(p, plan, static_cast<cudaStream_t>(stream));
+  p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  cudaError_t e = launch_spmv(p, plan, flags, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
 int nm_spmv(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* x,
             void* y, void* workspace, size_t workspace_bytes, void* stream) {
-  return nm_spmv_ex(values, masks, rows, cols, x, y, workspace, workspace_bytes, -1, 0, stream);
+  return nm_spmv_ex(values, masks, rows, cols, x, y, workspace, workspace_bytes, -1, 0,
+                    NM_FLAG_PDL, stream);
 }
 
 int nm_spmv_plan(int64_t rows, int64_t cols, int* variant, int* grid, int* warps) {
@@ -268,7 +270,7 @@ int nm_spmv_variant_count(void) { return spmv_variant_count(); }
 int dense_gemv_variant_count(void) { return gemv_variant_count(); }
 
 int dense_gemv_ex(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
-                  int variant, int grid, void* stream) {
+                  int variant, int grid, int flags, void* stream) {
   if (!W || !x || !y) return NM_ERR_NULL;
   if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 8 != 0 || ld < cols) return NM_ERR_SHAPE;
   if (!aligned(W, 16) || ld % 8 != 0 || !aligned(x, 16) || !aligned(y, 2)) return NM_ERR_ALIGN;
@@ -285,13 +287,14 @@ int dense_gemv_ex(const void* W, int64_t rows, int64_t cols, int64_t ld, const v
   p.x = static_cast<const __half*>(x);
   p.y = static_cast<__half*>(y);
   p.ld = ld;
-  cudaError_t e = launch_gemv(p, plan, static_cast<cudaStream_t>(stream));
+  p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  cudaError_t e = launch_gemv(p, plan, flags, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
 int dense_gemv(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
                void* stream) {
-  return dense_gemv_ex(W, rows, cols, ld, x, y, -1, 0, stream);
+  return dense_gemv_ex(W, rows, cols, ld, x, y, -1, 0, NM_FLAG_PDL, stream);
 }
 
 int64_t nm_check_masks(const uint32_t* masks, int64_t rows, int64_t cols, void* stream) {

@@ -98,6 +98,18 @@ __device__ __forceinline__ float fma_f16f16_f32(uint16_t a, uint16_t b, float c)
   return d;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled as soon as SMs free up, and wait for the previous kernel's
+// completion (and memory) before touching anything it may have written.
+// Both are no-ops when the launch does not use the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_previous() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -84,7 +84,10 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
 
   GemvCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
   GemvBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
   gemv_load<U>(A, lc, wr.se, T, p, br.r0, lane);
+  if (p.early_weights) pdl_wait_previous();  // x (and y) may come from the previous kernel
 
   for (int i = threadIdx.x; i < T * 64; i += NW * 32) {
     xs[i] = (i * 8 < p.cols) ? ld_keep_v4(p.x + (int64_t)i * 8) : make_uint4(0u, 0u, 0u, 0u);
@@ -130,13 +133,12 @@ size_t gemv_smem_bytes(int steps, int nw) {
 }
 
 template <int NW, int U>
-static cudaError_t launch_gemv_t(const GemvParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_gemv_t(const GemvParams& p, int grid, int flags, cudaStream_t stream) {
   static int smem_set[64] = {0};
   auto* k = gemv_kernel<NW, U>;
   cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
   if (e != cudaSuccess) return e;
-  k<<<grid, NW * 32, gemv_smem_bytes(p.steps, NW), stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k, grid, NW * 32, gemv_smem_bytes(p.steps, NW), stream, flags, p);
 }
 
 static const int kGemvVariants[][2] = {{16, 4}, {24, 2}, {16, 2}, {8, 8}};
@@ -147,12 +149,13 @@ int gemv_variant_warps(int variant) {
   return (variant >= 0 && variant < gemv_variant_count()) ? kGemvVariants[variant][0] : 0;
 }
 
-cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream) {
+cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, int flags,
+                        cudaStream_t stream) {
   switch (plan.variant) {
-    case 0: return launch_gemv_t<16, 4>(p, plan.grid, stream);
-    case 1: return launch_gemv_t<24, 2>(p, plan.grid, stream);
-    case 2: return launch_gemv_t<16, 2>(p, plan.grid, stream);
-    case 3: return launch_gemv_t<8, 8>(p, plan.grid, stream);
+    case 0: return launch_gemv_t<16, 4>(p, plan.grid, flags, stream);
+    case 1: return launch_gemv_t<24, 2>(p, plan.grid, flags, stream);
+    case 2: return launch_gemv_t<16, 2>(p, plan.grid, flags, stream);
+    case 3: return launch_gemv_t<8, 8>(p, plan.grid, flags, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -18,6 +18,7 @@ struct SpmvParams {
   int words;  // cols / 32
   int steps;  // ceil(words / 32): warp-steps per row
   int pitch;  // floats per row of the transposed x tile (multiple of 32, >= words)
+  int early_weights;  // 1: load the first weights before waiting on the previous kernel
 };
 
 struct SpmvPlan {
@@ -29,7 +30,8 @@ struct SpmvPlan {
 int spmv_variant_warps(int variant);
 int spmv_variant_count();
 size_t spmv_smem_bytes(int pitch, int nw);
-cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, cudaStream_t stream);
+cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
+                        cudaStream_t stream);
 
 // ---- dense -----------------------------------------------------------------
 struct GemvParams {
@@ -40,6 +42,7 @@ struct GemvParams {
   int64_t ld;
   int cols;
   int steps;  // ceil(cols / 512)
+  int early_weights;
 };
 
 struct GemvPlan {
@@ -51,7 +54,8 @@ struct GemvPlan {
 int gemv_variant_warps(int variant);
 int gemv_variant_count();
 size_t gemv_smem_bytes(int steps, int nw);
-cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, int flags,
+                        cudaStream_t stream);
 
 // ---- format ----------------------------------------------------------------
 cudaError_t launch_pack(const __half* W, int64_t rows, int64_t cols, int64_t ld, int M,
@@ -60,6 +64,28 @@ cudaError_t launch_unpack(const __half* values, const uint32_t* masks, int64_t r
                           int64_t cols, __half* W, int64_t ld, cudaStream_t stream);
 cudaError_t launch_check_masks(const uint32_t* masks, int64_t n_words,
                                unsigned long long* d_count, cudaStream_t stream);
+
+// Launch flags (same values as NM_FLAG_* in nm_spmv.h).
+constexpr int kFlagPdl = 1;
+
+// Launch `kernel` with the programmatic-stream-serialization attribute when
+// flags ask for it (the kernel may then start while the previous kernel on the
+// stream finishes; it waits for it with griddepcontrol.wait).
+template <typename Kernel, typename Params>
+inline cudaError_t launch_kernel(Kernel kernel, int grid, int block, size_t smem,
+                                 cudaStream_t stream, int flags, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (flags & kFlagPdl) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 // Sets the dynamic shared memory limit of `func` to the device maximum once
 // per device.

@@ -187,8 +187,11 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
 
   SpmvCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
   SpmvBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
   // Start the first weight loads before staging x so both latencies overlap.
   spmv_load<U>(A, lc, wr.se, T, p, br.r0, lane);
+  if (p.early_weights) pdl_wait_previous();  // x (and y) may come from the previous kernel
   stage_x<DEC>(xs, p.x, p.words, P, NW * 32);
   __syncthreads();
 
@@ -268,7 +271,10 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
   const uint32_t* vp = p.values + (g * 32 + lane) * 8;
 
   SpmvBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
   if (nfull > 0) load_steps<U>(A, vp, mp);
+  if (p.early_weights) pdl_wait_previous();  // x (and y) may come from the previous kernel
   stage_x<DEC>(xs, p.x, p.words, P, NW * 32);
   __syncthreads();
 
@@ -319,7 +325,7 @@ size_t spmv_smem_bytes(int pitch, int nw) {
 }
 
 template <int NW, int U, int DEC>
-static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, int flags, cudaStream_t stream) {
   static int smem_full[64] = {0}, smem_gen[64] = {0};
   const size_t smem = spmv_smem_bytes(p.pitch, NW);
   const int64_t block_steps = (p.rows + grid - 1) / grid * p.steps;
@@ -327,14 +333,12 @@ static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, cudaStream_t str
     auto* k = spmv_full_kernel<NW, U, DEC>;
     cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_full, 64);
     if (e != cudaSuccess) return e;
-    k<<<grid, NW * 32, smem, stream>>>(p);
-  } else {
-    auto* k = spmv_kernel<NW, U, DEC>;
-    cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_gen, 64);
-    if (e != cudaSuccess) return e;
-    k<<<grid, NW * 32, smem, stream>>>(p);
+    return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
   }
-  return cudaGetLastError();
+  auto* k = spmv_kernel<NW, U, DEC>;
+  cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_gen, 64);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
 }
 
 // (warps per block, steps in flight per warp, decode)
@@ -347,16 +351,17 @@ int spmv_variant_warps(int variant) {
   return (variant >= 0 && variant < spmv_variant_count()) ? kSpmvVariants[variant][0] : 0;
 }
 
-cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, cudaStream_t stream) {
+cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
+                        cudaStream_t stream) {
   switch (plan.variant) {
-    case 0: return launch_spmv_t<16, 4, 2>(p, plan.grid, stream);
-    case 1: return launch_spmv_t<24, 2, 2>(p, plan.grid, stream);
-    case 2: return launch_spmv_t<24, 2, 3>(p, plan.grid, stream);
-    case 3: return launch_spmv_t<24, 2, 1>(p, plan.grid, stream);
-    case 4: return launch_spmv_t<32, 1, 2>(p, plan.grid, stream);
-    case 5: return launch_spmv_t<16, 2, 2>(p, plan.grid, stream);
-    case 6: return launch_spmv_t<20, 3, 2>(p, plan.grid, stream);
-    case 7: return launch_spmv_t<20, 2, 2>(p, plan.grid, stream);
+    case 0: return launch_spmv_t<16, 4, 2>(p, plan.grid, flags, stream);
+    case 1: return launch_spmv_t<24, 2, 2>(p, plan.grid, flags, stream);
+    case 2: return launch_spmv_t<24, 2, 3>(p, plan.grid, flags, stream);
+    case 3: return launch_spmv_t<24, 2, 1>(p, plan.grid, flags, stream);
+    case 4: return launch_spmv_t<32, 1, 2>(p, plan.grid, flags, stream);
+    case 5: return launch_spmv_t<16, 2, 2>(p, plan.grid, flags, stream);
+    case 6: return launch_spmv_t<20, 3, 2>(p, plan.grid, flags, stream);
+    case 7: return launch_spmv_t<20, 2, 2>(p, plan.grid, flags, stream);
     default: return cudaErrorInvalidValue;
   }
 }

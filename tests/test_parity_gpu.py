@@ -143,7 +143,8 @@ def test_spmv_exact_arithmetic_every_plan(nm, orc, rows, cols):
         xd = to_dev(x)
         for variant in range(nm.nm_spmv_variant_count()):
             for grid in sorted({1, 2, 7, 152, rows}):
-                y = nm.nm_spmv(v, m, xd, variant=variant, grid=grid)
+                flags = (0, 1, 3)[(variant + grid) % 3]  # plain, PDL, PDL + early weights
+                y = nm.nm_spmv(v, m, xd, variant=variant, grid=grid, flags=flags)
                 got = from_dev(y)
                 bad = np.nonzero(got != expect)[0]
                 assert bad.size == 0, (N, M, variant, grid, bad[:5], got[bad[:5]], expect[bad[:5]])
@@ -176,6 +177,30 @@ def test_spmv_unit_vectors_exact(nm, orc):
             col = dense[:, j].copy()
             col[col == 0x8000] = 0x0000  # -0 * 1 + 0 accumulates to +0
             assert np.array_equal(y, col), (N, M, j)
+
+
+def test_chained_calls_with_pdl(nm):
+    """y of one call is x of the next, kernels back to back on one stream: with
+    programmatic dependent launch (and early weight loads) every call must
+    still see its predecessor's output -- the chain must match the plain one
+    bit for bit.  (|y| stays O(1): the gains are ~0.9 sparse, ~1.3 dense.)"""
+    n = 4096
+    _, x = gen(n, n, 17)
+    mats = [nm.nm_pack(to_dev(synth.weights(n, n, 0, synth.stream_id(17, i))), 2, 4)
+            for i in range(4)]
+    Wd = [to_dev(synth.weights(n, n, 0, synth.stream_id(18, i))) for i in range(3)]
+    outs = {}
+    for flags in (0, 1, 3):
+        cur = to_dev(x)
+        for rep in range(3):
+            for v, m in mats:
+                cur = nm.nm_spmv(v, m, cur, flags=flags)
+            for Wi in Wd:
+                cur = nm.dense_gemv(Wi, cur, flags=flags)
+        got = from_dev(cur)
+        assert np.all(np.isfinite(got.view(np.float16)))
+        outs[flags] = got
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[3])
 
 
 def test_spmv_deterministic(nm):
@@ -291,7 +316,7 @@ def test_argument_errors(nm):
     assert L.nm_spmv(P(v), P(m), rows, cols, P(xd) + 8, P(y), None, 0, s) == 4
     assert L.nm_spmv(P(v), P(m), rows, cols, P(xd), P(xd), None, 0, s) == 7
     assert L.nm_spmv(P(v), P(m), 0, cols, P(xd), P(y), None, 0, s) == 0
-    assert L.nm_spmv_ex(P(v), P(m), rows, cols, P(xd), P(y), None, 0, 99, 0, s) == 2
+    assert L.nm_spmv_ex(P(v), P(m), rows, cols, P(xd), P(y), None, 0, 99, 0, 1, s) == 2
     vv, mm = torch.empty_like(v), torch.empty_like(m)
     for N, M in [(1, 4), (2, 8), (3, 4), (32, 64)]:
         assert L.nm_pack(P(Wd), rows, cols, cols, N, M, P(vv), P(mm), s) == 3
