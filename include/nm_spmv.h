@@ -177,6 +177,29 @@ int dense_gemv_ex(const void *W, int64_t rows, int64_t cols, int64_t ld,
  * ------------------------------------------------------------------------- */
 int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * nm_check_masks_noalloc -- the same count as nm_check_masks, without any
+ * device allocation.  The paper has no counterpart to this entry point; it
+ * exists for callers that must not allocate device memory while they run --
+ * a serving process whose memory is all handed to its own caching allocator
+ * or arena at start-up, or a latency-critical loop where a stream-ordered
+ * allocation could stall on the memory pool.
+ *   Scratch: a fixed array inside the library's device image (32 KB + 8 B),
+ *   held by every GPU that loads the library until the process exits.
+ *   Limit: rows * cols / 32 <= NM_CHECK_NOALLOC_MAX_WORDS mask words;
+ *   larger inputs return -NM_ERR_WORKSPACE without launching anything.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the array: calls that overlap on the GPU (different
+ *   streams or host threads at the same time) race and must be serialised by
+ *   the caller.  Each call writes every scratch slot it reads, so nothing
+ *   carries over from one call to the next.
+ *   Returns the number of words whose popcount is not 16, or a negative
+ *   nm_status; host-synchronous (waits for the stream).
+ * ------------------------------------------------------------------------- */
+#define NM_CHECK_NOALLOC_MAX_WORDS ((int64_t)67108864) /* 4096 blocks x 16384 words */
+int64_t nm_check_masks_noalloc(const uint32_t *masks, int64_t rows, int64_t cols, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

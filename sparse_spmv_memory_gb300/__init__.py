@@ -25,7 +25,8 @@ __all__ = [
     "NMError", "lib", "library_path",
     "nm_status_string", "nm_values_bytes", "nm_masks_bytes", "nm_spmv_workspace_bytes",
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
-    "nm_check_masks", "nm_spmv_variant_count", "dense_gemv_variant_count",
+    "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
+    "dense_gemv_variant_count",
 ]
 
 NM_OK = 0
@@ -79,6 +80,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "dense_gemv_ex": ([P, I64, I64, I64, P, P, I32, I32, I32, P], I32),
         "dense_gemv_variant_count": ([], I32),
         "nm_check_masks": ([P, I64, I64, P], I64),
+        "nm_check_masks_noalloc": ([P, I64, I64, P], I64),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -239,4 +241,15 @@ def nm_check_masks(masks, cols: int, stream=None) -> int:
     r = lib().nm_check_masks(_ptr(masks), masks.shape[0], cols, _stream(stream))
     if r < 0:
         raise NMError(-r, "nm_check_masks")
+    return r
+
+
+def nm_check_masks_noalloc(masks, cols: int, stream=None) -> int:
+    """As nm_check_masks, for callers that must not allocate device memory:
+    the scratch is a fixed array inside the library (limit: rows * cols / 32
+    <= 67,108,864 words).  Calls overlapping on the GPU race on that array."""
+    _need_cuda(masks)
+    r = lib().nm_check_masks_noalloc(_ptr(masks), masks.shape[0], cols, _stream(stream))
+    if r < 0:
+        raise NMError(-r, "nm_check_masks_noalloc")
     return r

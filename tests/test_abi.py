@@ -16,6 +16,7 @@ def declared_functions():
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"^\s*#[^\n]*", "", text, flags=re.M)  # preprocessor lines
         names += re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{}]*\)\s*;", text)
     return sorted(set(names))
 
