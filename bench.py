@@ -56,6 +56,9 @@ WORKLOADS = {
     "single_4096": [("W", 4096, 4096)],
 }
 PATTERNS = [(2, 4), (4, 8), (8, 16), (16, 32)]
+# decoder layers of each model (one step = one token through all of them)
+LAYERS = {"llama33_70b_layer": 80, "qwen3_32b_layer": 64, "llama31_8b_layer": 32,
+          "pattern_sweep": 32, "single_4096": 64}
 
 
 # ---------------------------------------------------------------------------
@@ -625,7 +628,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama33_70b_layer")
     ap.add_argument("--pattern", default="2:4")
-    ap.add_argument("--layers", type=int, default=80)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="logical layers per step (default: the model's layer count)")
     ap.add_argument("--slots", type=int, default=16, help="physical sparse layer slots")
     ap.add_argument("--dense-slots", type=int, default=8)
     ap.add_argument("--no-dense", dest="dense", action="store_false")
@@ -639,6 +643,8 @@ def parse(argv=None):
                          "dependency wait")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     a = ap.parse_args(argv)
+    if a.layers is None:
+        a.layers = LAYERS[a.workload]
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     return a

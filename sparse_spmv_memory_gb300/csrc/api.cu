@@ -86,8 +86,10 @@ int64_t gemv_steps(int64_t cols) { return (cols + 511) / 512; }
 // positions (where the launch's fixed start-up cost weighs more) the
 // {24 warps, 2 steps, fp32 x} variant is ahead.
 int default_spmv_variant(int64_t rows = 0, int64_t cols = 0) {
-  return rows * cols >= ((int64_t)1 << 27) ? 6 : 3;
+  return rows * cols >= ((int64_t)1 << 27) ? 1 : 0;
 }
+
+// The dense baseline's fastest variant on every decode-layer shape measured.
 int default_gemv_variant() { return 0; }
 
 // Builds the sparse launch plan; returns NM_OK or a status.
@@ -100,7 +102,8 @@ int make_spmv_plan(int64_t rows, int64_t cols, int variant, int grid, SpmvPlan* 
   const int nw = spmv_variant_warps(variant);
   const int64_t words = cols / 32;
   const int pitch = spmv_pitch(words);
-  if (spmv_smem_bytes(pitch, nw) > (size_t)d.smem_optin) return NM_ERR_SHAPE;
+  const size_t smem = spmv_smem_bytes(pitch, nw);
+  if (smem > (size_t)d.smem_optin) return NM_ERR_SHAPE;
   if (grid <= 0) grid = d.sms;  // one resident block per SM
   if (grid > rows) grid = (int)rows;
   plan->variant = variant;

@@ -341,9 +341,13 @@ static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, int flags, cudaS
   return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
 }
 
-// (warps per block, steps in flight per warp, decode)
-static const int kSpmvVariants[][3] = {{16, 4, 2}, {24, 2, 2}, {24, 2, 3}, {24, 2, 1},
-                                       {32, 1, 2}, {16, 2, 2}, {20, 3, 2}, {20, 2, 2}};
+// (warps per block, steps in flight per warp, decode).  Every variant runs
+// one resident block per SM.  Sweeps on GB300 over the decode-layer shapes put
+// variant 0 ahead below ~134M weight positions and variant 1 above; the others
+// stay for tuning and so the tests cover more block shapes.  (Blocks sized for
+// two per SM, one or two launched per SM, were slower on every shape.)
+static const int kSpmvVariants[][3] = {{24, 2, 1}, {20, 3, 2}, {16, 4, 2},
+                                       {24, 2, 2}, {24, 2, 3}, {16, 2, 1}};
 
 int spmv_variant_count() { return (int)(sizeof(kSpmvVariants) / sizeof(kSpmvVariants[0])); }
 
@@ -354,14 +358,13 @@ int spmv_variant_warps(int variant) {
 cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
                         cudaStream_t stream) {
   switch (plan.variant) {
-    case 0: return launch_spmv_t<16, 4, 2>(p, plan.grid, flags, stream);
-    case 1: return launch_spmv_t<24, 2, 2>(p, plan.grid, flags, stream);
-    case 2: return launch_spmv_t<24, 2, 3>(p, plan.grid, flags, stream);
-    case 3: return launch_spmv_t<24, 2, 1>(p, plan.grid, flags, stream);
-    case 4: return launch_spmv_t<32, 1, 2>(p, plan.grid, flags, stream);
-    case 5: return launch_spmv_t<16, 2, 2>(p, plan.grid, flags, stream);
-    case 6: return launch_spmv_t<20, 3, 2>(p, plan.grid, flags, stream);
-    case 7: return launch_spmv_t<20, 2, 2>(p, plan.grid, flags, stream);
+#define NM_SPMV_CASE(i)                                                                 \
+  case i:                                                                              \
+    return launch_spmv_t<kSpmvVariants[i][0], kSpmvVariants[i][1], kSpmvVariants[i][2]>( \
+        p, plan.grid, flags, stream);
+    NM_SPMV_CASE(0) NM_SPMV_CASE(1) NM_SPMV_CASE(2) NM_SPMV_CASE(3) NM_SPMV_CASE(4)
+    NM_SPMV_CASE(5)
+#undef NM_SPMV_CASE
     default: return cudaErrorInvalidValue;
   }
 }
