@@ -84,9 +84,11 @@ int64_t gemv_steps(int64_t cols) { return (cols + 511) / 512; }
 // Measured on GB300 over the decode-layer shapes: the {20 warps, 3 steps in
 // flight, fp16 x} variant streams large matrices fastest; below ~134M weight
 // positions (where the launch's fixed start-up cost weighs more) the
-// {24 warps, 2 steps, fp32 x} variant is ahead.
+// {24 warps, 2 steps, fp32 x} variant is ahead, and below ~33M the
+// {28 warps, 1 step, fp32 x} one.
 int default_spmv_variant(int64_t rows = 0, int64_t cols = 0) {
-  return rows * cols >= ((int64_t)1 << 27) ? 1 : 0;
+  const int64_t n = rows * cols;
+  return n >= ((int64_t)1 << 27) ? 1 : (n >= ((int64_t)1 << 25) ? 0 : 6);
 }
 
 // The dense baseline's fastest variant on every decode-layer shape measured.

@@ -343,11 +343,13 @@ static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, int flags, cudaS
 
 // (warps per block, steps in flight per warp, decode).  Every variant runs
 // one resident block per SM.  Sweeps on GB300 over the decode-layer shapes put
-// variant 0 ahead below ~134M weight positions and variant 1 above; the others
-// stay for tuning and so the tests cover more block shapes.  (Blocks sized for
-// two per SM, one or two launched per SM, were slower on every shape.)
-static const int kSpmvVariants[][3] = {{24, 2, 1}, {20, 3, 2}, {16, 4, 2},
-                                       {24, 2, 2}, {24, 2, 3}, {16, 2, 1}};
+// variant 6 ahead below ~33M weight positions (more warps hide the decode's
+// latencies when each warp has only a few steps), variant 0 up to ~134M and
+// variant 1 above; the others stay for tuning and so the tests cover more
+// block shapes.  (Blocks sized for two per SM, one or two launched per SM,
+// were slower on every shape.)
+static const int kSpmvVariants[][3] = {{24, 2, 1}, {20, 3, 2}, {16, 4, 2}, {24, 2, 2},
+                                       {24, 2, 3}, {16, 2, 1}, {28, 1, 1}};
 
 int spmv_variant_count() { return (int)(sizeof(kSpmvVariants) / sizeof(kSpmvVariants[0])); }
 
@@ -363,7 +365,7 @@ cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
     return launch_spmv_t<kSpmvVariants[i][0], kSpmvVariants[i][1], kSpmvVariants[i][2]>( \
         p, plan.grid, flags, stream);
     NM_SPMV_CASE(0) NM_SPMV_CASE(1) NM_SPMV_CASE(2) NM_SPMV_CASE(3) NM_SPMV_CASE(4)
-    NM_SPMV_CASE(5)
+    NM_SPMV_CASE(5) NM_SPMV_CASE(6)
 #undef NM_SPMV_CASE
     default: return cudaErrorInvalidValue;
   }
