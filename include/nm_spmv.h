@@ -125,6 +125,37 @@ int nm_spmv(const void *values, const uint32_t *masks, int64_t rows, int64_t col
             void *stream);
 
 /* ---------------------------------------------------------------------------
+ * nm_spmm -- Y = W X for a small batch of tokens (1..8), W in the packed
+ * format.  Decoding several tokens at once (small-batch serving, speculative
+ * decoding) is the step between the batch-one SpMV and the prefill SpMM the
+ * pages contrast it with (news.bitwarelabs.com summary, "What's new").  Each
+ * mask word is decoded once for the whole batch.
+ *   X : device fp16 [batch][ldx], 16-byte aligned, ldx % 8 == 0, ldx >= cols;
+ *       token j's activations are X[j][0..cols).
+ *   Y : device fp16 [batch][ldy], ldy >= rows; Y[j][r] = sum_c W[r][c] X[j][c].
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *       nm_spmm_workspace_bytes(rows, cols, batch) bytes (0 when a whole row's
+ *       x tile fits in one block's shared memory, else fp32 partial sums of
+ *       column slices).  May be NULL when that is 0.
+ * Same arithmetic, rounding and determinism as nm_spmv; each column of Y is
+ * within the same tolerance of the exact product (and equals nm_spmv's
+ * result whenever the sums are exact).  batch outside 1..8 -> NM_ERR_SHAPE;
+ * a short workspace -> NM_ERR_WORKSPACE.  Y must not overlap any input or the
+ * workspace.
+ * ------------------------------------------------------------------------- */
+size_t nm_spmm_workspace_bytes(int64_t rows, int64_t cols, int batch);
+int nm_spmm(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+            const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
+            void *workspace, size_t workspace_bytes, void *stream);
+/* Explicit plan: kernel variant (< 0: default), grid (<= 0: default), column
+ * slices (<= 0: the fewest that fit), launch flags as for nm_spmv_ex. */
+int nm_spmm_variant_count(void);
+int nm_spmm_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+               const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
+               void *workspace, size_t workspace_bytes, int variant, int grid, int slices,
+               int flags, void *stream);
+
+/* ---------------------------------------------------------------------------
  * dense_gemv -- the dense baseline y = W x on an unpruned fp16 matrix
  * (aimodeling.com article, "The Kernel Is the Other Half of the Answer":
  * speedups are stated against dense decoding throughput).

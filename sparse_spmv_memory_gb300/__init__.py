@@ -26,7 +26,7 @@ __all__ = [
     "nm_status_string", "nm_values_bytes", "nm_masks_bytes", "nm_spmv_workspace_bytes",
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
-    "dense_gemv_variant_count",
+    "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
 ]
 
 NM_OK = 0
@@ -81,6 +81,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "dense_gemv_variant_count": ([], I32),
         "nm_check_masks": ([P, I64, I64, P], I64),
         "nm_check_masks_noalloc": ([P, I64, I64, P], I64),
+        "nm_spmm_workspace_bytes": ([I64, I64, I32], SZ),
+        "nm_spmm": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
+        "nm_spmm_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, I32, P], I32),
+        "nm_spmm_variant_count": ([], I32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -213,6 +217,48 @@ def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int 
                           NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "nm_spmv")
     return y
+
+
+def nm_spmm_workspace_bytes(rows: int, cols: int, batch: int) -> int:
+    return lib().nm_spmm_workspace_bytes(rows, cols, batch)
+
+
+def nm_spmm_variant_count() -> int:
+    return lib().nm_spmm_variant_count()
+
+
+def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int = -1,
+            grid: int = 0, slices: int = 0, flags: int | None = None, cols: int | None = None):
+    """Y = W X for a batch of 1..8 tokens: X fp16 [batch][ldx] (first ``cols``
+    columns used), Y fp16 [batch][ldy].  A workspace of
+    nm_spmm_workspace_bytes(...) bytes is allocated with PyTorch when needed
+    and none is given."""
+    torch = _torch()
+    _need_cuda(values, masks, X)
+    rows = masks.shape[0]
+    batch, ldx = X.shape
+    cols = ldx if cols is None else cols
+    if X.stride(1) != 1 or (Y is not None and Y.stride(1) != 1):
+        raise ValueError("X and Y must have unit column stride")
+    if Y is None:
+        Y = torch.empty((batch, rows), dtype=torch.float16, device=X.device)
+    _need_cuda(Y, workspace)
+    L = lib()
+    if workspace is None:
+        need = L.nm_spmm_workspace_bytes(rows, cols, batch) if slices <= 0 else \
+            slices * batch * rows * 4
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant < 0 and grid <= 0 and slices <= 0 and flags is None:
+        st = L.nm_spmm(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), batch,
+                       _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream(stream))
+    else:
+        st = L.nm_spmm_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), batch,
+                          _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, variant, grid, slices,
+                          NM_FLAG_PDL if flags is None else flags, _stream(stream))
+    _check(st, "nm_spmm")
+    return Y
 
 
 def dense_gemv(W, x, y=None, cols: int | None = None, stream=None, variant: int = -1,

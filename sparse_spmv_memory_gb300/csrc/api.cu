@@ -138,6 +138,47 @@ int make_gemv_plan(int64_t rows, int64_t cols, int variant, int grid, GemvPlan* 
   return NM_OK;
 }
 
+// Sparse small-batch plan: padded batch, column slices so the x tile fits.
+int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid, int slices,
+                   SpmmPlan* plan, SpmmParams* p) {
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  if (variant < 0) variant = 0;
+  if (variant >= spmm_variant_count()) return NM_ERR_SHAPE;
+  const int nw = spmm_variant_warps(variant);
+  const int bp = spmm_padded_batch(batch);
+  const int64_t words = cols / 32;
+  const int64_t T = (words + 31) / 32;
+  auto pitch_for = [&](int64_t S) { return (int)((T + S - 1) / S * 32); };
+  if (slices <= 0) {
+    int64_t S = 1;
+    while (S < T && spmm_smem_bytes(pitch_for(S), nw, bp) > (size_t)d.smem_optin) ++S;
+    slices = (int)S;
+  }
+  if (slices > T || spmm_smem_bytes(pitch_for(slices), nw, bp) > (size_t)d.smem_optin)
+    return NM_ERR_SHAPE;
+  if (grid <= 0) grid = d.sms;
+  int64_t bps = grid / slices;
+  if (bps < 1) bps = 1;
+  if (bps > rows) bps = rows;
+  plan->variant = variant;
+  plan->grid = (int)(bps * slices);
+  plan->bp = bp;
+  plan->sms = d.sms;
+  plan->warps = nw;
+  p->rows = rows;
+  p->words = (int)words;
+  p->steps = (int)T;
+  p->slices = slices;
+  p->pitch = pitch_for(slices);
+  p->batch = batch;
+  return NM_OK;
+}
+
+size_t spmm_workspace_for(const SpmmParams& p) {
+  return p.slices > 1 ? (size_t)p.slices * p.batch * p.rows * sizeof(float) : 0;
+}
+
 int check_spmv_args(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                     const void* x, const void* y) {
   if (!values || !masks || !x || !y) return NM_ERR_NULL;
@@ -300,6 +341,63 @@ int dense_gemv_ex(const void* W, int64_t rows, int64_t cols, int64_t ld, const v
 int dense_gemv(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
                void* stream) {
   return dense_gemv_ex(W, rows, cols, ld, x, y, -1, 0, NM_FLAG_PDL, stream);
+}
+
+size_t nm_spmm_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || batch < 1 || batch > 8)
+    return 0;
+  SpmmPlan plan;
+  SpmmParams p;
+  if (make_spmm_plan(rows, cols, batch, -1, 0, 0, &plan, &p) != NM_OK) return 0;
+  return spmm_workspace_for(p);
+}
+
+int nm_spmm_variant_count(void) { return spmm_variant_count(); }
+
+int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+               const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
+               size_t workspace_bytes, int variant, int grid, int slices, int flags,
+               void* stream) {
+  if (!values || !masks || !X || !Y) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || batch < 1 || batch > 8 ||
+      ldx < cols || ldy < rows)
+    return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
+      !aligned(Y, 2) || (workspace && !aligned(workspace, 16)))
+    return NM_ERR_ALIGN;
+  if (rows == 0) return NM_OK;
+  const size_t yb = (size_t)((batch - 1) * ldy + rows) * 2;
+  const size_t xb = (size_t)((batch - 1) * ldx + cols) * 2;
+  if (overlap(Y, yb, values, (size_t)rows * cols) || overlap(Y, yb, masks, (size_t)rows * cols / 8) ||
+      overlap(Y, yb, X, xb) || overlap(Y, yb, workspace, workspace_bytes))
+    return NM_ERR_ALIAS;
+  SpmmPlan plan;
+  SpmmParams p;
+  int st = make_spmm_plan(rows, cols, batch, variant, grid, slices, &plan, &p);
+  if (st != NM_OK) return st;
+  const size_t need = spmm_workspace_for(p);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return NM_ERR_WORKSPACE;
+  if (need > 0 && (overlap(workspace, need, values, (size_t)rows * cols) ||
+                   overlap(workspace, need, masks, (size_t)rows * cols / 8) ||
+                   overlap(workspace, need, X, xb)))
+    return NM_ERR_ALIAS;
+  p.values = static_cast<const uint32_t*>(values);
+  p.masks = masks;
+  p.X = static_cast<const __half*>(X);
+  p.ldx = ldx;
+  p.Y = static_cast<__half*>(Y);
+  p.ldy = ldy;
+  p.partial = static_cast<float*>(workspace);
+  p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  cudaError_t e = launch_spmm(p, plan, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmm(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* X,
+            int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace, size_t workspace_bytes,
+            void* stream) {
+  return nm_spmm_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace, workspace_bytes,
+                    -1, 0, 0, NM_FLAG_PDL, stream);
 }
 
 int64_t nm_check_masks(const uint32_t* masks, int64_t rows, int64_t cols, void* stream) {

@@ -57,6 +57,39 @@ size_t gemv_smem_bytes(int steps, int nw);
 cudaError_t launch_gemv(const GemvParams& p, const GemvPlan& plan, int flags,
                         cudaStream_t stream);
 
+// ---- small-batch sparse ------------------------------------------------------
+struct SpmmParams {
+  const uint32_t* values;
+  const uint32_t* masks;
+  const __half* X;  // [batch][ldx]
+  int64_t ldx;
+  __half* Y;        // [batch][ldy]
+  int64_t ldy;
+  float* partial;   // [slices][batch][rows] fp32 when slices > 1
+  int64_t rows;
+  int words;   // cols / 32
+  int steps;   // ceil(words / 32): warp-steps per row
+  int slices;  // column slices
+  int pitch;   // x-tile slots per row (>= 32 * steps of the widest slice)
+  int batch;   // 1..8
+  int early_weights;
+};
+
+struct SpmmPlan {
+  int variant;
+  int grid;
+  int bp;    // padded batch: 2, 4 or 8
+  int sms;
+  int warps;
+};
+
+int spmm_variant_count();
+int spmm_variant_warps(int variant);
+int spmm_padded_batch(int batch);
+size_t spmm_smem_bytes(int pitch, int nw, int bp);
+cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
+                        cudaStream_t stream);
+
 // ---- format ----------------------------------------------------------------
 cudaError_t launch_pack(const __half* W, int64_t rows, int64_t cols, int64_t ld, int M,
                         __half* values, uint32_t* masks, cudaStream_t stream);
@@ -71,9 +104,9 @@ constexpr int kFlagPdl = 1;
 // Launch `kernel` with the programmatic-stream-serialization attribute when
 // flags ask for it (the kernel may then start while the previous kernel on the
 // stream finishes; it waits for it with griddepcontrol.wait).
-template <typename Kernel, typename Params>
+template <typename Kernel, typename... Args>
 inline cudaError_t launch_kernel(Kernel kernel, int grid, int block, size_t smem,
-                                 cudaStream_t stream, int flags, const Params& p) {
+                                 cudaStream_t stream, int flags, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
@@ -84,7 +117,7 @@ inline cudaError_t launch_kernel(Kernel kernel, int grid, int block, size_t smem
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (flags & kFlagPdl) ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Sets the dynamic shared memory limit of `func` to the device maximum once

@@ -78,4 +78,46 @@ __device__ __forceinline__ void combine_cut_rows(int64_t F, int T, const float* 
   store(rl, sum);
 }
 
+// The same two steps for N values per row (one per token of a batch):
+// pf/pl hold N floats per warp, store receives the row and its N sums.
+template <int N, typename Store>
+__device__ __forceinline__ void finish_row_n(int64_t row, const float (&v)[N], const WarpRange& wr,
+                                             int T, int warp, int lane, float* pf, float* pl,
+                                             Store&& store) {
+  if (lane != 0) return;
+  const int64_t beg = row * T, end = beg + T;
+  if (beg >= wr.sb && end <= wr.se) {
+    store(row, v);
+  } else {
+    float* dst = (row == wr.sb / T) ? pf + warp * N : pl + warp * N;
+#pragma unroll
+    for (int j = 0; j < N; ++j) dst[j] = v[j];
+  }
+}
+
+template <int NW, int N, typename Store>
+__device__ __forceinline__ void combine_cut_rows_n(int64_t F, int T, const float* pf,
+                                                   const float* pl, Store&& store) {
+  const int t = threadIdx.x;
+  if (t >= NW) return;
+  const WarpRange wr = warp_range<NW>(F, t);
+  if (wr.sb == wr.se) return;
+  const int64_t rf = wr.sb / T, rl = (wr.se - 1) / T;
+  const bool cut_at_end = (wr.se % T) != 0;
+  const bool first_contributor = (rl != rf) || (wr.sb % T == 0);
+  if (!(cut_at_end && first_contributor)) return;
+  float sum[N];
+  const float* own = (rl == rf) ? pf + t * N : pl + t * N;
+#pragma unroll
+  for (int j = 0; j < N; ++j) sum[j] = own[j];
+  for (int u = t + 1; u < NW; ++u) {
+    const WarpRange wu = warp_range<NW>(F, u);
+    if (wu.sb == wu.se) continue;
+#pragma unroll
+    for (int j = 0; j < N; ++j) sum[j] += pf[u * N + j];  // row rl is warp u's first row
+    if (wu.se >= (rl + 1) * T) break;
+  }
+  store(rl, sum);
+}
+
 }  // namespace nmk

@@ -1,0 +1,305 @@
+// spmm.cu -- small-batch N:M bitmask SpMM, Y = W X for 1..8 tokens (sm_103a).
+//
+// Decoding several tokens at once (small-batch serving, speculative decoding)
+// turns the batch-one product of the SparseDecoding pages (aimodeling.com
+// article, "The Kernel Is the Other Half of the Answer"; news.bitwarelabs.com
+// summary, "What's new": decoding is SpMV-bound, prefill SpMM-bound) into a
+// product with a handful of right-hand sides.  The weights still dominate the
+// traffic, so the kernel streams them exactly as nm_spmv does and decodes each
+// mask word once for the whole batch:
+//  * the x tile holds, for every (bit b, mask word w), one slot of BP fp16
+//    values -- the BP tokens' x at column 32w + b (BP = 2, 4 or 8; tokens past
+//    the batch are zero).  Lanes of a warp hold consecutive words, so one
+//    4/8/16-byte shared load per nonzero feeds all BP FMAs without a bank
+//    conflict;
+//  * the same two-chain bfind scan as nm_spmv (values 15..8 from the top bit,
+//    0..7 from the bit-reversed mask; exhausted chains read zero pad rows);
+//  * one mixed-precision fp16*fp16+fp32 FMA per nonzero and token;
+//  * rows split over blocks and row-steps over warps as in nm_spmv
+//    (split.cuh), with BP sums per row.
+// When the tile of a whole row does not fit in shared memory (long rows with
+// a large batch), the columns are cut into S slices of whole warp-steps, the
+// grid is shared among the slices, each block writes fp32 partial sums for
+// its slice to the caller's workspace, and a second kernel adds the S
+// partials in slice order (deterministic) and rounds to fp16.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device.cuh"
+#include "kernels.h"
+#include "split.cuh"
+
+namespace nmk {
+
+template <int BP>
+__device__ __forceinline__ void lds_slot(uint32_t addr, uint32_t (&r)[BP / 2]) {
+  if constexpr (BP == 2) {
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r[0]) : "r"(addr));
+  } else if constexpr (BP == 4) {
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+  } else {
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+  }
+}
+
+__device__ __forceinline__ uint16_t half_of(uint32_t pair, int hi) {
+  return hi ? (uint16_t)(pair >> 16) : (uint16_t)(pair & 0xFFFFu);
+}
+
+// One mask word, all BP tokens: 16 trips as two chains of 8.
+template <int BP>
+__device__ __forceinline__ void decode_word_batch(uint32_t m, const uint32_t (&v)[8],
+                                                  uint32_t col_addr, uint32_t row_bytes,
+                                                  float (&a)[2][BP]) {
+  uint32_t mh = m;
+  uint32_t ml = bit_reverse(m);
+  const uint32_t top = col_addr + 31u * row_bytes;
+  const uint32_t neg_row = 0u - row_bytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bh = msb_index(mh);
+    const uint32_t bl = msb_index(ml);
+    const uint32_t ah = col_addr + bh * row_bytes;  // ~0u -> pad row 0
+    const uint32_t al = top + bl * neg_row;         // ~0u -> pad row 33
+    mh ^= bit_at(bh);
+    ml ^= bit_at(bl);
+    uint32_t xh[BP / 2], xl[BP / 2];
+    lds_slot<BP>(ah, xh);
+    lds_slot<BP>(al, xl);
+    const int kh = 15 - k, kl = k;
+    const uint16_t wh = half_of(v[kh >> 1], kh & 1);
+    const uint16_t wl = half_of(v[kl >> 1], kl & 1);
+#pragma unroll
+    for (int j = 0; j < BP; ++j) {
+      a[1][j] = fma_f16f16_f32(wh, half_of(xh[j >> 1], j & 1), a[1][j]);
+      a[0][j] = fma_f16f16_f32(wl, half_of(xl[j >> 1], j & 1), a[0][j]);
+    }
+  }
+}
+
+template <int U>
+struct SpmmBatch {
+  uint32_t m[U];
+  uint32_t v[U][8];
+};
+
+struct SpmmCursor {
+  int64_t s;    // next step of the block's flattened (row, step) range
+  int64_t row;  // its local row
+  int t;        // its step within the slice's part of the row
+};
+
+__device__ __forceinline__ void advance(SpmmCursor& c, int T) {
+  ++c.s;
+  if (++c.t == T) {
+    c.t = 0;
+    ++c.row;
+  }
+}
+
+template <int U>
+__device__ __forceinline__ void spmm_load(SpmmBatch<U>& bt, SpmmCursor& c, int64_t se, int T,
+                                          const SpmmParams& p, int64_t r0, int w0, int wend,
+                                          int lane) {
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int w = w0 + c.t * 32 + lane;
+    if (c.s < se && w < wend) {
+      const int64_t word = (r0 + c.row) * (int64_t)p.words + w;
+      bt.m[i] = ld_stream_u32(p.masks + word);
+      ld_stream_v8(p.values + word * 8, bt.v[i]);
+    } else {
+      bt.m[i] = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bt.v[i][j] = 0u;
+    }
+    if (c.s < se) advance(c, T);
+  }
+}
+
+template <int NW, int U, int BP>
+__global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
+  extern __shared__ __align__(16) float smem[];
+  const int P = p.pitch;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] fp16
+  float* pf = smem + 34 * P * (BP / 2);                 // [NW][BP]
+  float* pl = pf + NW * BP;                             // [NW][BP]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bps = gridDim.x / p.slices;  // blocks per slice
+  const int sl = blockIdx.x / bps, c = blockIdx.x - sl * bps;
+  const int64_t r0 = p.rows * c / bps, r1 = p.rows * (c + 1) / bps;
+  const int ts0 = (int)((int64_t)p.steps * sl / p.slices);
+  const int ts1 = (int)((int64_t)p.steps * (sl + 1) / p.slices);
+  const int T = ts1 - ts0;              // warp-steps per row in this slice
+  const int w0 = ts0 * 32;              // first mask word of the slice
+  const int wend = min(ts1 * 32, p.words);
+  const int64_t F = (r1 - r0) * T;
+  const WarpRange wr = warp_range<NW>(F, warp);
+
+  SpmmCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  SpmmBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
+  spmm_load<U>(A, lc, wr.se, T, p, r0, w0, wend, lane);
+  if (p.early_weights) pdl_wait_previous();  // X (and Y, the workspace) may be the previous kernel's
+
+  // Stage the slice of X: tile[1 + b][wl][j] = X[j][32 (w0 + wl) + b].
+  const int nthreads = NW * 32;
+  uint32_t* tile32 = reinterpret_cast<uint32_t*>(smem);
+  for (int i = threadIdx.x; i < P * (BP / 2); i += nthreads) {
+    tile32[i] = 0u;
+    tile32[33 * P * (BP / 2) + i] = 0u;
+  }
+  for (int task = threadIdx.x; task < P * BP; task += nthreads) {
+    const int j = task / P, wl = task - j * P;
+    const int w = w0 + wl;
+    uint32_t h[16];
+    if (w < wend && j < p.batch) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.X + (int64_t)j * p.ldx) + (int64_t)w * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = ld_keep_v4(src + q);
+        h[4 * q] = u.x;
+        h[4 * q + 1] = u.y;
+        h[4 * q + 2] = u.z;
+        h[4 * q + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) h[q] = 0u;
+    }
+#pragma unroll
+    for (int b = 0; b < 32; ++b)
+      tile[((int64_t)(1 + b) * P + wl) * BP + j] = half_of(h[b >> 1], b & 1);
+  }
+  __syncthreads();
+
+  const uint32_t row_bytes = (uint32_t)P * BP * 2u;
+  const uint32_t tile_base = smem_addr(tile) + row_bytes;  // row b = 0
+  auto store = [&](int64_t row, const float (&v)[BP]) {
+    const int64_t gr = r0 + row;
+    if (p.slices == 1) {
+#pragma unroll
+      for (int j = 0; j < BP; ++j)
+        if (j < p.batch) p.Y[(int64_t)j * p.ldy + gr] = __float2half_rn(v[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < BP; ++j)
+        if (j < p.batch) p.partial[((int64_t)sl * p.batch + j) * p.rows + gr] = v[j];
+    }
+  };
+
+  SpmmCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  float a[2][BP];
+#pragma unroll
+  for (int j = 0; j < BP; ++j) a[0][j] = a[1][j] = 0.f;
+
+  auto compute = [&](SpmmBatch<U>& bt) {
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (cc.s < wr.se) {
+        const uint32_t col_addr = tile_base + (uint32_t)(cc.t * 32 + lane) * (BP * 2u);
+        decode_word_batch<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
+        if (cc.t == T - 1 || cc.s == wr.se - 1) {
+          float v[BP];
+#pragma unroll
+          for (int j = 0; j < BP; ++j) {
+            v[j] = warp_sum(a[0][j] + a[1][j]);
+            a[0][j] = a[1][j] = 0.f;
+          }
+          finish_row_n<BP>(cc.row, v, wr, T, warp, lane, pf, pl, store);
+        }
+        advance(cc, T);
+      }
+    }
+  };
+
+  while (cc.s < wr.se) {
+    spmm_load<U>(B, lc, wr.se, T, p, r0, w0, wend, lane);
+    compute(A);
+    if (cc.s >= wr.se) break;
+    spmm_load<U>(A, lc, wr.se, T, p, r0, w0, wend, lane);
+    compute(B);
+  }
+
+  __syncthreads();
+  combine_cut_rows_n<NW, BP>(F, T, pf, pl, store);
+}
+
+// Y[j][r] = sum over slices s (in order) of partial[s][j][r], rounded to fp16.
+__global__ void __launch_bounds__(256) spmm_combine_kernel(const float* __restrict__ partial,
+                                                           int slices, int batch, int64_t rows,
+                                                           __half* __restrict__ Y, int64_t ldy) {
+  pdl_launch_dependents();
+  pdl_wait_previous();
+  const int64_t n = (int64_t)batch * rows;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t j = i / rows, r = i - j * rows;
+    float s = 0.f;
+    for (int k = 0; k < slices; ++k) s += partial[((int64_t)k * batch + j) * rows + r];
+    Y[j * ldy + r] = __float2half_rn(s);
+  }
+}
+
+size_t spmm_smem_bytes(int pitch, int nw, int bp) {
+  return (size_t)34 * pitch * bp * 2 + 2 * (size_t)nw * bp * sizeof(float);
+}
+
+int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8); }
+
+// (warps per block, steps in flight per warp)
+static const int kSpmmVariants[][2] = {{16, 2}, {20, 2}, {12, 3}, {24, 1}};
+
+int spmm_variant_count() { return (int)(sizeof(kSpmmVariants) / sizeof(kSpmmVariants[0])); }
+
+int spmm_variant_warps(int variant) {
+  return (variant >= 0 && variant < spmm_variant_count()) ? kSpmmVariants[variant][0] : 0;
+}
+
+template <int NW, int U, int BP>
+static cudaError_t launch_spmm_t(const SpmmParams& p, int grid, int flags, cudaStream_t stream) {
+  static int smem_set[64] = {0};
+  auto* k = spmm_kernel<NW, U, BP>;
+  cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k, grid, NW * 32, spmm_smem_bytes(p.pitch, NW, BP), stream, flags, p);
+}
+
+template <int NW, int U>
+static cudaError_t launch_spmm_bp(const SpmmParams& p, int bp, int grid, int flags,
+                                  cudaStream_t stream) {
+  switch (bp) {
+    case 2: return launch_spmm_t<NW, U, 2>(p, grid, flags, stream);
+    case 4: return launch_spmm_t<NW, U, 4>(p, grid, flags, stream);
+    case 8: return launch_spmm_t<NW, U, 8>(p, grid, flags, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
+                        cudaStream_t stream) {
+  cudaError_t e;
+  switch (plan.variant) {
+#define NM_SPMM_CASE(i)                                                                 \
+  case i:                                                                              \
+    e = launch_spmm_bp<kSpmmVariants[i][0], kSpmmVariants[i][1]>(p, plan.bp, plan.grid, \
+                                                                  flags, stream);       \
+    break;
+    NM_SPMM_CASE(0) NM_SPMM_CASE(1) NM_SPMM_CASE(2) NM_SPMM_CASE(3)
+#undef NM_SPMM_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess || p.slices == 1) return e;
+  const int64_t n = (int64_t)p.batch * p.rows;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4 * plan.sms) blocks = 4 * plan.sms;
+  return launch_kernel(spmm_combine_kernel, blocks > 0 ? blocks : 1, 256, 0, stream, flags,
+                       p.partial, p.slices, p.batch, p.rows, p.Y, p.ldy);
+}
+
+}  // namespace nmk

@@ -163,3 +163,28 @@ def test_lane_words_stay_inside_the_row(cols):
     for b in range(-1, 32):
         for row in (1 + b, 1 + (31 - b)):
             assert 0 <= row * pitch + (words - 1) < 34 * pitch
+
+
+@pytest.mark.parametrize("rows,T", [(1, 1), (7, 3), (300, 8), (57, 28), (4096, 25)])
+def test_spmm_slices_cover_every_step_once(rows, T):
+    """Small-batch SpMM: the grid is shared by S column slices (blocks per
+    slice = grid // S, at most rows); slice s covers warp-steps
+    [T*s//S, T*(s+1)//S) of every row.  Every (row, step) must be read by
+    exactly one block and every (row, slice) written once."""
+    for S in sorted({1, 2, 3, T}):
+        if S > T:
+            continue
+        for grid in (1, 7, 152):
+            bps = max(1, min(grid // S, rows))
+            G = bps * S
+            reads, writes = {}, {}
+            for b in range(G):
+                sl, c = divmod(b, bps)
+                r0, r1 = rows * c // bps, rows * (c + 1) // bps
+                ts0, ts1 = T * sl // S, T * (sl + 1) // S
+                for r in range(r0, r1):
+                    for t in range(ts0, ts1):
+                        reads[(r, t)] = reads.get((r, t), 0) + 1
+                    writes[(r, sl)] = writes.get((r, sl), 0) + 1
+            assert len(reads) == rows * T and all(v == 1 for v in reads.values())
+            assert len(writes) == rows * S and all(v == 1 for v in writes.values())

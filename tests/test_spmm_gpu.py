@@ -1,0 +1,152 @@
+"""GPU parity of the small-batch SpMM (Y = W X, 1..8 tokens) against the CPU
+oracle: every column of Y is an SpMV, so the oracle's packed SpMV of each
+token is the reference.  Within the stated tolerance on random inputs; bit
+for bit on exact-arithmetic inputs for every kernel variant, column-slice
+count and grid size."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import f16_to_f64, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def nm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_spmv_memory_gb300 import _build
+    _build.build()
+    import sparse_spmv_memory_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.Oracle()
+
+
+def gen(rows, cols, batch, tag, exact=False):
+    sw = synth.stream_id(40, tag, rows, cols, batch, 0)
+    sx = synth.stream_id(40, tag, rows, cols, batch, 1)
+    if exact:
+        W = synth.int_f16((rows, cols), 0, sw, -8, 8, -6)
+        X = synth.int_f16((batch, cols), 0, sx, -2, 2, 0)
+    else:
+        W = synth.weights(rows, cols, 0, sw)
+        X = synth.normal_f16((batch, cols), 0, sx, synth.X_SIGMA)
+    return W, X
+
+
+def oracle_spmm(orc, ov, om, cols, X):
+    ys, ss = [], []
+    for j in range(X.shape[0]):
+        y, s = orc.spmv_f64(ov, om, cols, X[j])
+        ys.append(y)
+        ss.append(s)
+    return np.stack(ys), np.stack(ss)
+
+
+def dev_masks(om):
+    return torch.from_numpy(om.view(np.int32)).cuda()
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (33, 1056), (300, 4096), (129, 14336), (64, 5120)])
+@pytest.mark.parametrize("batch", [1, 2, 3, 5, 8])
+def test_spmm_within_tolerance(nm, orc, rows, cols, batch):
+    W, X = gen(rows, cols, batch, 1)
+    N, M = [(2, 4), (4, 8), (8, 16), (16, 32)][batch % 4]
+    ov, om = orc.prune_pack(W, N, M)
+    Y = from_dev(nm.nm_spmm(to_dev(ov), dev_masks(om), to_dev(X)))
+    ref, s = oracle_spmm(orc, ov, om, cols, X)
+    err = np.abs(f16_to_f64(Y) - ref)
+    assert np.all(err <= oracle.tolerance(s)), (rows, cols, batch, err.max())
+
+
+@pytest.mark.parametrize("rows,cols", [(33, 1056), (300, 4096), (129, 14336)])
+def test_spmm_exact_every_plan(nm, orc, rows, cols):
+    """Exact sums: Y must equal the oracle's fp16 rounding bit for bit for every
+    variant, column-slice count (partials summed by the second kernel) and grid."""
+    T = (cols // 32 + 31) // 32
+    for batch in (2, 4, 7):
+        W, X = gen(rows, cols, batch, 2, exact=True)
+        ov, om = orc.prune_pack(W, 2, 4)
+        ref, _ = oracle_spmm(orc, ov, om, cols, X)
+        expect = np.stack([orc.round_f16(r) for r in ref])
+        v, m, Xd = to_dev(ov), dev_masks(om), to_dev(X)
+        # the fewest slices whose x tile fits (more are always allowed)
+        ws = nm.nm_spmm_workspace_bytes(rows, cols, batch)
+        s_min = ws // (batch * rows * 4) if ws else 1
+        for variant in range(nm.nm_spmm_variant_count()):
+            for slices in sorted({0, 1, min(2, T), min(3, T), T}):
+                if 0 < slices < s_min:
+                    with pytest.raises(nm.NMError) as e:
+                        nm.nm_spmm(v, m, Xd, variant=variant, slices=slices)
+                    assert e.value.status == 2  # does not fit: refused, nothing launched
+                    continue
+                for grid in (0, 7):
+                    flags = (0, 1, 3)[(variant + slices + grid) % 3]
+                    Y = nm.nm_spmm(v, m, Xd, variant=variant, grid=grid, slices=slices,
+                                   flags=flags)
+                    got = from_dev(Y)
+                    assert np.array_equal(got, expect), (batch, variant, slices, grid)
+
+
+def test_spmm_batch_one_equals_spmv_on_exact_inputs(nm, orc):
+    rows, cols = 500, 8192
+    W, X = gen(rows, cols, 1, 3, exact=True)
+    v, m = nm.nm_pack(to_dev(W), 8, 16)
+    Xd = to_dev(X)
+    y1 = from_dev(nm.nm_spmv(v, m, Xd[0]))
+    Y = from_dev(nm.nm_spmm(v, m, Xd))
+    assert np.array_equal(Y[0], y1)
+
+
+def test_spmm_strided_and_workspace(nm, orc):
+    rows, cols, batch = 200, 2048, 6
+    ldx, ldy = cols + 64, rows + 9
+    Wf, Xw = gen(rows, ldx, batch, 4)
+    W = np.ascontiguousarray(Wf[:, :cols])
+    ov, om = orc.prune_pack(W, 4, 8)
+    v, m = to_dev(ov), dev_masks(om)
+    Xd = to_dev(Xw)
+    Yd = torch.full((batch, ldy), 3.0, dtype=torch.float16, device="cuda")
+    nm.nm_spmm(v, m, Xd, Y=Yd, cols=cols, slices=2)
+    got = from_dev(Yd)
+    ref, s = oracle_spmm(orc, ov, om, cols, np.ascontiguousarray(Xw[:, :cols]))
+    assert np.all(np.abs(f16_to_f64(got[:, :rows]) - ref) <= oracle.tolerance(s))
+    assert np.all(got[:, rows:] == np.float16(3.0).view(np.uint16))  # untouched
+    # a slice plan needs the workspace: too small is refused before any launch
+    L = nm.lib()
+    s_ = torch.cuda.current_stream().cuda_stream
+    st = L.nm_spmm_ex(v.data_ptr(), m.data_ptr(), rows, cols, Xd.data_ptr(), ldx, batch,
+                      Yd.data_ptr(), ldy, None, 0, 0, 0, 2, 1, s_)
+    assert st == 5
+    assert L.nm_spmm_ex(v.data_ptr(), m.data_ptr(), rows, cols, Xd.data_ptr(), ldx, 9,
+                        Yd.data_ptr(), ldy, None, 0, 0, 0, 1, 1, s_) == 2   # batch > 8
+
+
+def test_spmm_long_rows_need_slices(nm):
+    # batch 8 on the 70B down projection: the x tile of a whole row does not fit
+    assert nm.nm_spmm_workspace_bytes(8192, 28672, 8) > 0
+    assert nm.nm_spmm_workspace_bytes(8192, 8192, 2) == 0
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(8192, 28672, 8), (57344, 8192, 4), (4096, 14336, 8)])
+def test_spmm_full_size_sampled_rows(nm, orc, rows, cols, batch):
+    W = synth.weights(rows, cols, 0, synth.stream_id(41, rows, cols))
+    X = synth.normal_f16((batch, cols), 0, synth.stream_id(42, rows, cols), synth.X_SIGMA)
+    v, m = nm.nm_pack(to_dev(W), 2, 4)
+    Y = from_dev(nm.nm_spmm(v, m, to_dev(X)))
+    ids = synth.sample_rows(rows, 48, 0, synth.stream_id(43, rows))
+    ov, om = orc.prune_pack(np.ascontiguousarray(W[ids]), 2, 4)
+    ref, s = oracle_spmm(orc, ov, om, cols, X)
+    err = np.abs(f16_to_f64(Y[:, ids]) - ref)
+    assert np.all(err <= oracle.tolerance(s)), err.max()
