@@ -271,7 +271,7 @@ def oracle_sample(mats, pattern, seconds: float):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def make_dense(mats, device):
+def make_dense(mats, device, batch=1):
     import torch
     import synth
     dense, xs = [], []
@@ -280,7 +280,9 @@ def make_dense(mats, device):
         synth.normal_f16_into(host.data_ptr(), rows * cols, 0, synth.stream_id(2, mi, 0),
                               synth.WEIGHT_SIGMA)
         dense.append(host.to(device, non_blocking=True).view(torch.float16))
-        xh = synth.activations(cols, 0, synth.stream_id(2, mi, 1))
+        xh = np.stack([synth.activations(cols, 0, synth.stream_id(2, mi, 1) if j == 0
+                                         else synth.stream_id(2, mi, 1, j))
+                       for j in range(batch)])
         xs.append(torch.from_numpy(xh.view(np.int16)).to(device).view(torch.float16))
     torch.cuda.synchronize()
     return dense, xs
@@ -309,11 +311,13 @@ def dense_slots(dense, slots):
 
 
 class Step:
-    """The calls of one decode step over `layers` logical layers."""
+    """The calls of one decode step over `layers` logical layers, for a batch
+    of `batch` tokens (1: nm_spmv / dense_gemv; 2..8: nm_spmm, and cuBLAS as
+    the dense reference since dense_gemv is batch-one)."""
 
-    def __init__(self, nm, mats, layers, device, flags=None):
+    def __init__(self, nm, mats, layers, device, flags=None, batch=1):
         import torch
-        self.nm, self.mats, self.layers, self.flags = nm, mats, layers, flags
+        self.nm, self.mats, self.layers, self.flags, self.batch = nm, mats, layers, flags, batch
         self.x_off, self.y_off = [], []
         xo = yo = 0
         for _, rows, cols in mats:
@@ -323,47 +327,74 @@ class Step:
             yo += rows
         self.x_per_layer, self.y_per_layer = xo, yo
         # per-layer inputs and outputs, contiguous so one copy moves a whole step
-        self.x_all = torch.empty((layers, xo), dtype=torch.float16, device=device)
-        self.y_all = torch.empty((layers, yo), dtype=torch.float16, device=device)
+        self.x_all = torch.empty((layers, batch, xo), dtype=torch.float16, device=device)
+        self.y_all = torch.empty((layers, batch, yo), dtype=torch.float16, device=device)
+        self.ws = None
+        if batch > 1:
+            need = max(nm.nm_spmm_workspace_bytes(r, c, batch) for _, r, c in mats)
+            if need:
+                self.ws = torch.empty(need, dtype=torch.uint8, device=device)
+            self.dense_out = [torch.empty((batch, r), dtype=torch.float16, device=device)
+                              for _, r, _ in mats]
 
     def fill_x(self, xs):
+        """xs[i]: [batch][cols] (or [cols]) activations of matrix i, reused by every layer."""
         for i, x in enumerate(xs):
-            self.x_all[:, self.x_off[i]:self.x_off[i] + x.numel()] = x
+            self.x_all[:, :, self.x_off[i]:self.x_off[i] + x.shape[-1]] = x
 
     def x(self, layer, i):
         _, rows, cols = self.mats[i]
-        return self.x_all[layer, self.x_off[i]:self.x_off[i] + cols]
+        v = self.x_all[layer, :, self.x_off[i]:self.x_off[i] + cols]
+        return v[0] if self.batch == 1 else v
 
     def y(self, layer, i):
         _, rows, cols = self.mats[i]
-        return self.y_all[layer, self.y_off[i]:self.y_off[i] + rows]
+        v = self.y_all[layer, :, self.y_off[i]:self.y_off[i] + rows]
+        return v[0] if self.batch == 1 else v
 
-    def run_sparse(self, slots, on_launch=None):
-        nm = self.nm
+    def call_sparse(self, v, m, l, i):
+        if self.batch == 1:
+            self.nm.nm_spmv(v, m, self.x(l, i), y=self.y(l, i), flags=self.flags)
+        else:
+            self.nm.nm_spmm(v, m, self.x(l, i), Y=self.y(l, i), workspace=self.ws,
+                            flags=self.flags)
+
+    def run_sparse(self, slots):
         for l in range(self.layers):
             slot = slots[l % len(slots)]
             for i, (v, m) in enumerate(slot):
-                if on_launch:
-                    on_launch(i, 0)
-                nm.nm_spmv(v, m, self.x(l, i), y=self.y(l, i), flags=self.flags)
-                if on_launch:
-                    on_launch(i, 1)
+                self.call_sparse(v, m, l, i)
 
     def run_dense(self, slots):
+        import torch
         nm = self.nm
         for l in range(self.layers):
             slot = slots[l % len(slots)]
             for i, W in enumerate(slot):
-                nm.dense_gemv(W, self.x(l, i), y=self.y(l, i), flags=self.flags)
+                if self.batch == 1:
+                    nm.dense_gemv(W, self.x(l, i), y=self.y(l, i), flags=self.flags)
+                else:
+                    torch.mm(self.x(l, i), W.t(), out=self.dense_out[i])
 
     def bytes_sparse(self):
-        return self.layers * sum(sparse_bytes(r, c) for _, r, c in self.mats)
+        B = self.batch
+        return self.layers * sum(sparse_bytes(r, c) + (B - 1) * 2 * (r + c) for _, r, c in self.mats)
 
     def bytes_dense(self):
-        return self.layers * sum(dense_bytes(r, c) for _, r, c in self.mats)
+        B = self.batch
+        return self.layers * sum(dense_bytes(r, c) + (B - 1) * 2 * (r + c) for _, r, c in self.mats)
 
     def calls(self):
         return self.layers * len(self.mats)
+
+    def launches(self):
+        """Kernels per step: one per call, plus the slice-combining kernel of
+        every nm_spmm call whose rows are cut into column slices."""
+        if self.batch == 1:
+            return self.calls()
+        extra = sum(1 for _, r, c in self.mats
+                    if self.nm.nm_spmm_workspace_bytes(r, c, self.batch) > 0)
+        return self.layers * (len(self.mats) + extra)
 
 
 def time_graph(fn, steps, warmup, stream, clock=None):
@@ -404,13 +435,12 @@ def time_per_matrix(step, slots, stream, reps):
     """µs per call of each matrix: a CUDA graph of `step.layers` calls of that
     matrix alone (cycling the slots, so every call streams from HBM), timed
     with CUDA events over `reps` replays after warm-up."""
-    nm = step.nm
     out = {}
     for i in range(len(step.mats)):
         def fn(i=i):
             for l in range(step.layers):
                 v, m = slots[l % len(slots)][i]
-                nm.nm_spmv(v, m, step.x(l, i), y=step.y(l, i), flags=step.flags)
+                step.call_sparse(v, m, l, i)
         per, total = time_graph(fn, reps, 3, stream)
         out[i] = [t * 1e3 / step.layers for t in per]  # us per call, per replay
     return out
@@ -430,8 +460,9 @@ def run_gpu(args):
     peak, peak_kind = hbm_peak()
 
     t_setup = time.time()
-    dense, xs = make_dense(mats, device)
-    step = Step(nm, mats, layers, device, flags=None if args.flags < 0 else args.flags)
+    dense, xs = make_dense(mats, device, args.batch)
+    step = Step(nm, mats, layers, device, flags=None if args.flags < 0 else args.flags,
+                batch=args.batch)
     step.fill_x(xs)
     setup_s = time.time() - t_setup
 
@@ -512,7 +543,7 @@ def run_gpu(args):
         "dtype": "fp16 in/out, fp32 accumulate",
         "data": "synthetic (seeded N(0,0.02) fp16 weights, top-N |w| per M-group; N(0,1) fp16 x)",
         "config": {
-            "workload": (f"{args.workload} x{layers} layers, batch 1, "
+            "workload": (f"{args.workload} x{layers} layers, batch {args.batch}, "
                          + ", ".join(f"{n} {r}x{c}" for n, r, c in mats)),
             "pattern": f"{head[0]}:{head[1]}",
             "calls_per_step": step.calls(),
@@ -526,7 +557,7 @@ def run_gpu(args):
                     "p90": round(float(np.percentile(per, 90)), 4)},
         "pct_peak": {"of_measured" if peak_kind == "measured" else "of_fallback":
                      round(gbs / world / peak, 4), "of_nominal_7900": round(gbs / world / NOMINAL_HBM_GBS, 4)},
-        "gpu_launches": step.calls() * k,
+        "gpu_launches": step.launches() * k,
     }
     # per-matrix µs per call (graphs of one matrix, CUDA events)
     calls = {}
@@ -568,7 +599,8 @@ def run_gpu(args):
         d_ms = dtotal / dk * 1e3
         out["dense"] = {"ms_per_step": round(d_ms, 4),
                         "GB_s": round(step.bytes_dense() * dk / dtotal / 1e9, 1),
-                        "physical_slots": args.dense_slots}
+                        "physical_slots": args.dense_slots,
+                        "kernel": "dense_gemv" if args.batch == 1 else "cuBLAS via torch.mm"}
         out["speedup_vs_dense"] = round(d_ms / (total / k * 1e3), 4)
         out["speedup_ideal"] = round(step.bytes_dense() / step_bytes, 4)
     xb = step.x_all.numel() * 2
@@ -582,7 +614,7 @@ def run_gpu(args):
     out["clocks"] = clocks
     out["setup_s"] = round(setup_s, 1)
 
-    if rank == 0 and world == 1 and args.cpu:
+    if rank == 0 and world == 1 and args.cpu and args.batch == 1:
         _, nb, dt, desc = oracle_sample(mats, head, args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
@@ -628,6 +660,9 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama33_70b_layer")
     ap.add_argument("--pattern", default="2:4")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="tokens per step: 1 = nm_spmv (the headline); 2..8 = nm_spmm, with "
+                         "cuBLAS (torch.mm) as the dense reference")
     ap.add_argument("--layers", type=int, default=None,
                     help="logical layers per step (default: the model's layer count)")
     ap.add_argument("--slots", type=int, default=16, help="physical sparse layer slots")
@@ -643,6 +678,8 @@ def parse(argv=None):
                          "dependency wait")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     a = ap.parse_args(argv)
+    if not 1 <= a.batch <= 8:
+        ap.error("--batch must be in 1..8")
     if a.layers is None:
         a.layers = LAYERS[a.workload]
     if a.warmup < 3:

@@ -148,8 +148,12 @@ int nm_spmm(const void *values, const uint32_t *masks, int64_t rows, int64_t col
             const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
             void *workspace, size_t workspace_bytes, void *stream);
 /* Explicit plan: kernel variant (< 0: default), grid (<= 0: default), column
- * slices (<= 0: the fewest that fit), launch flags as for nm_spmv_ex. */
+ * slices (<= 0: the fewest that fit), launch flags as for nm_spmv_ex.  The
+ * workspace such a plan needs is nm_spmm_workspace_bytes_ex(rows, cols,
+ * batch, variant, slices) (0 also for a plan that cannot run). */
 int nm_spmm_variant_count(void);
+size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant,
+                                  int slices);
 int nm_spmm_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
                void *workspace, size_t workspace_bytes, int variant, int grid, int slices,

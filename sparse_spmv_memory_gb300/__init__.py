@@ -82,6 +82,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_check_masks": ([P, I64, I64, P], I64),
         "nm_check_masks_noalloc": ([P, I64, I64, P], I64),
         "nm_spmm_workspace_bytes": ([I64, I64, I32], SZ),
+        "nm_spmm_workspace_bytes_ex": ([I64, I64, I32, I32, I32], SZ),
         "nm_spmm": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
         "nm_spmm_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, I32, P], I32),
         "nm_spmm_variant_count": ([], I32),
@@ -245,8 +246,7 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
     _need_cuda(Y, workspace)
     L = lib()
     if workspace is None:
-        need = L.nm_spmm_workspace_bytes(rows, cols, batch) if slices <= 0 else \
-            slices * batch * rows * 4
+        need = L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, slices)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

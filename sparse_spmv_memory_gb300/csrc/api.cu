@@ -143,19 +143,22 @@ int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid,
                    SpmmPlan* plan, SpmmParams* p) {
   DeviceInfo d;
   if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
-  if (variant < 0) variant = 0;
+  // measured on GB300 (70B layer shapes): 20 warps x 2 steps up to batch 4,
+  // 16 warps x 2 steps at batch 5-8
+  if (variant < 0) variant = batch <= 4 ? 1 : 0;
   if (variant >= spmm_variant_count()) return NM_ERR_SHAPE;
   const int nw = spmm_variant_warps(variant);
+  const int xf = spmm_variant_xf(variant);
   const int bp = spmm_padded_batch(batch);
   const int64_t words = cols / 32;
   const int64_t T = (words + 31) / 32;
   auto pitch_for = [&](int64_t S) { return (int)((T + S - 1) / S * 32); };
   if (slices <= 0) {
     int64_t S = 1;
-    while (S < T && spmm_smem_bytes(pitch_for(S), nw, bp) > (size_t)d.smem_optin) ++S;
+    while (S < T && spmm_smem_bytes(pitch_for(S), nw, bp, xf) > (size_t)d.smem_optin) ++S;
     slices = (int)S;
   }
-  if (slices > T || spmm_smem_bytes(pitch_for(slices), nw, bp) > (size_t)d.smem_optin)
+  if (slices > T || spmm_smem_bytes(pitch_for(slices), nw, bp, xf) > (size_t)d.smem_optin)
     return NM_ERR_SHAPE;
   if (grid <= 0) grid = d.sms;
   int64_t bps = grid / slices;
@@ -343,13 +346,18 @@ int dense_gemv(const void* W, int64_t rows, int64_t cols, int64_t ld, const void
   return dense_gemv_ex(W, rows, cols, ld, x, y, -1, 0, NM_FLAG_PDL, stream);
 }
 
-size_t nm_spmm_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant,
+                                  int slices) {
   if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || batch < 1 || batch > 8)
     return 0;
   SpmmPlan plan;
   SpmmParams p;
-  if (make_spmm_plan(rows, cols, batch, -1, 0, 0, &plan, &p) != NM_OK) return 0;
+  if (make_spmm_plan(rows, cols, batch, variant, 0, slices, &plan, &p) != NM_OK) return 0;
   return spmm_workspace_for(p);
+}
+
+size_t nm_spmm_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+  return nm_spmm_workspace_bytes_ex(rows, cols, batch, -1, 0);
 }
 
 int nm_spmm_variant_count(void) { return spmm_variant_count(); }

@@ -86,7 +86,8 @@ struct SpmmPlan {
 int spmm_variant_count();
 int spmm_variant_warps(int variant);
 int spmm_padded_batch(int batch);
-size_t spmm_smem_bytes(int pitch, int nw, int bp);
+int spmm_variant_xf(int variant);
+size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf);
 cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
                         cudaStream_t stream);
 

@@ -14,7 +14,10 @@
 //    conflict;
 //  * the same two-chain bfind scan as nm_spmv (values 15..8 from the top bit,
 //    0..7 from the bit-reversed mask; exhausted chains read zero pad rows);
-//  * one mixed-precision fp16*fp16+fp32 FMA per nonzero and token;
+//  * per nonzero either one mixed-precision fp16*fp16+fp32 FMA per token
+//    (XF 0: fp16 slots) or one fp16->fp32 convert of the weight and one
+//    packed fp32x2 FMA per two tokens (XF 1: fp32 slots, twice the shared
+//    memory, half the FMA instructions at batch 4-8);
 //  * rows split over blocks and row-steps over warps as in nm_spmv
 //    (split.cuh), with BP sums per row.
 // When the tile of a whole row does not fit in shared memory (long rows with
@@ -43,6 +46,41 @@ __device__ __forceinline__ void lds_slot(uint32_t addr, uint32_t (&r)[BP / 2]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
   }
+}
+
+// fp32 slot loads: BP floats as BP/2 packed pairs.  A 32-byte slot (BP 8) is
+// read as two 16-byte halves; word w keeps its halves swapped when bit 2 of w
+// is set (swz = 16), so the 8 lanes of a quarter-warp hit disjoint banks.
+template <int BP>
+__device__ __forceinline__ void lds_slot_f32(uint32_t addr, uint32_t swz,
+                                             unsigned long long (&r)[BP / 2]) {
+  if constexpr (BP == 2) {
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(r[0]) : "r"(addr));
+  } else if constexpr (BP == 4) {
+    asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];" : "=l"(r[0]), "=l"(r[1]) : "r"(addr));
+  } else {
+    asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];" : "=l"(r[0]), "=l"(r[1]) : "r"(addr + swz));
+    asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];"
+                 : "=l"(r[2]), "=l"(r[3])
+                 : "r"(addr + (16u - swz)));
+  }
+}
+
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long splat2(float v) {
+  const unsigned long long u = __float_as_uint(v);
+  return (u << 32) | u;
+}
+
+__device__ __forceinline__ float pair_lo(unsigned long long p) { return __uint_as_float((uint32_t)p); }
+__device__ __forceinline__ float pair_hi(unsigned long long p) {
+  return __uint_as_float((uint32_t)(p >> 32));
 }
 
 __device__ __forceinline__ uint16_t half_of(uint32_t pair, int hi) {
@@ -76,6 +114,76 @@ __device__ __forceinline__ void decode_word_batch(uint32_t m, const uint32_t (&v
     for (int j = 0; j < BP; ++j) {
       a[1][j] = fma_f16f16_f32(wh, half_of(xh[j >> 1], j & 1), a[1][j]);
       a[0][j] = fma_f16f16_f32(wl, half_of(xl[j >> 1], j & 1), a[0][j]);
+    }
+  }
+}
+
+// As decode_word_batch, with fp32 slots: a[c][q] packs tokens 2q, 2q+1.
+template <int BP>
+__device__ __forceinline__ void decode_word_batch_f32(uint32_t m, const uint32_t (&v)[8],
+                                                      uint32_t col_addr, uint32_t row_bytes,
+                                                      uint32_t swz,
+                                                      unsigned long long (&a)[2][BP / 2]) {
+  uint32_t mh = m;
+  uint32_t ml = bit_reverse(m);
+  const uint32_t top = col_addr + 31u * row_bytes;
+  const uint32_t neg_row = 0u - row_bytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bh = msb_index(mh);
+    const uint32_t bl = msb_index(ml);
+    const uint32_t ah = col_addr + bh * row_bytes;
+    const uint32_t al = top + bl * neg_row;
+    mh ^= bit_at(bh);
+    ml ^= bit_at(bl);
+    unsigned long long xh[BP / 2], xl[BP / 2];
+    lds_slot_f32<BP>(ah, swz, xh);
+    lds_slot_f32<BP>(al, swz, xl);
+    const int kh = 15 - k, kl = k;
+    const float2 fh = half2_bits_to_float2(v[kh >> 1]);
+    const float2 fl = half2_bits_to_float2(v[kl >> 1]);
+    const unsigned long long wh = splat2((kh & 1) ? fh.y : fh.x);
+    const unsigned long long wl = splat2((kl & 1) ? fl.y : fl.x);
+#pragma unroll
+    for (int q = 0; q < BP / 2; ++q) {
+      a[1][q] = ffma2(wh, xh[q], a[1][q]);
+      a[0][q] = ffma2(wl, xl[q], a[0][q]);
+    }
+  }
+}
+
+// fp32 slots with scalar FMAs (XF 2): one convert of the weight and one fp32
+// FMA per token, no half extraction.
+template <int BP>
+__device__ __forceinline__ void decode_word_batch_f32s(uint32_t m, const uint32_t (&v)[8],
+                                                       uint32_t col_addr, uint32_t row_bytes,
+                                                       uint32_t swz, float (&a)[2][BP]) {
+  uint32_t mh = m;
+  uint32_t ml = bit_reverse(m);
+  const uint32_t top = col_addr + 31u * row_bytes;
+  const uint32_t neg_row = 0u - row_bytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bh = msb_index(mh);
+    const uint32_t bl = msb_index(ml);
+    const uint32_t ah = col_addr + bh * row_bytes;
+    const uint32_t al = top + bl * neg_row;
+    mh ^= bit_at(bh);
+    ml ^= bit_at(bl);
+    unsigned long long xh[BP / 2], xl[BP / 2];
+    lds_slot_f32<BP>(ah, swz, xh);
+    lds_slot_f32<BP>(al, swz, xl);
+    const int kh = 15 - k, kl = k;
+    const float2 fh = half2_bits_to_float2(v[kh >> 1]);
+    const float2 fl = half2_bits_to_float2(v[kl >> 1]);
+    const float wh = (kh & 1) ? fh.y : fh.x;
+    const float wl = (kl & 1) ? fl.y : fl.x;
+#pragma unroll
+    for (int j = 0; j < BP; ++j) {
+      const float xhj = (j & 1) ? pair_hi(xh[j >> 1]) : pair_lo(xh[j >> 1]);
+      const float xlj = (j & 1) ? pair_hi(xl[j >> 1]) : pair_lo(xl[j >> 1]);
+      a[1][j] = fmaf(wh, xhj, a[1][j]);
+      a[0][j] = fmaf(wl, xlj, a[0][j]);
     }
   }
 }
@@ -120,12 +228,14 @@ __device__ __forceinline__ void spmm_load(SpmmBatch<U>& bt, SpmmCursor& c, int64
   }
 }
 
-template <int NW, int U, int BP>
+template <int NW, int U, int BP, int XF>
 __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;
-  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] fp16
-  float* pf = smem + 34 * P * (BP / 2);                 // [NW][BP]
+  constexpr int kSlotWords = XF ? BP : BP / 2;          // 32-bit words per slot
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] fp16 (XF 0)
+  float* tile_f = smem;                                 // [34][P][BP] fp32 (XF 1)
+  float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
   float* pl = pf + NW * BP;                             // [NW][BP]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -150,9 +260,9 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   // Stage the slice of X: tile[1 + b][wl][j] = X[j][32 (w0 + wl) + b].
   const int nthreads = NW * 32;
   uint32_t* tile32 = reinterpret_cast<uint32_t*>(smem);
-  for (int i = threadIdx.x; i < P * (BP / 2); i += nthreads) {
+  for (int i = threadIdx.x; i < P * kSlotWords; i += nthreads) {
     tile32[i] = 0u;
-    tile32[33 * P * (BP / 2) + i] = 0u;
+    tile32[33 * P * kSlotWords + i] = 0u;
   }
   for (int task = threadIdx.x; task < P * BP; task += nthreads) {
     const int j = task / P, wl = task - j * P;
@@ -173,12 +283,21 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
       for (int q = 0; q < 16; ++q) h[q] = 0u;
     }
 #pragma unroll
-    for (int b = 0; b < 32; ++b)
-      tile[((int64_t)(1 + b) * P + wl) * BP + j] = half_of(h[b >> 1], b & 1);
+    for (int b = 0; b < 32; ++b) {
+      const int jp = (XF && BP == 8) ? (((j >> 2) ^ ((wl >> 2) & 1)) << 2) | (j & 3) : j;
+      const int64_t at = ((int64_t)(1 + b) * P + wl) * BP + jp;
+      if (XF) {
+        const float2 f = half2_bits_to_float2(h[b >> 1]);
+        tile_f[at] = (b & 1) ? f.y : f.x;
+      } else {
+        tile[at] = half_of(h[b >> 1], b & 1);
+      }
+    }
   }
   __syncthreads();
 
-  const uint32_t row_bytes = (uint32_t)P * BP * 2u;
+  const uint32_t row_bytes = (uint32_t)P * kSlotWords * 4u;
+  const uint32_t swz = ((lane >> 2) & 1) ? 16u : 0u;  // local word bit 2 == lane bit 2
   const uint32_t tile_base = smem_addr(tile) + row_bytes;  // row b = 0
   auto store = [&](int64_t row, const float (&v)[BP]) {
     const int64_t gr = r0 + row;
@@ -194,23 +313,37 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   };
 
   SpmmCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
-  float a[2][BP];
+  float a[2][BP];                   // XF 0
+  unsigned long long a2[2][BP / 2];  // XF 1: packed pairs of tokens
 #pragma unroll
   for (int j = 0; j < BP; ++j) a[0][j] = a[1][j] = 0.f;
+#pragma unroll
+  for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
 
   auto compute = [&](SpmmBatch<U>& bt) {
 #pragma unroll
     for (int i = 0; i < U; ++i) {
       if (cc.s < wr.se) {
-        const uint32_t col_addr = tile_base + (uint32_t)(cc.t * 32 + lane) * (BP * 2u);
-        decode_word_batch<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
+        const uint32_t col_addr = tile_base + (uint32_t)(cc.t * 32 + lane) * (kSlotWords * 4u);
+        if (XF == 1)
+          decode_word_batch_f32<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a2);
+        else if (XF == 2)
+          decode_word_batch_f32s<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a);
+        else
+          decode_word_batch<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
         if (cc.t == T - 1 || cc.s == wr.se - 1) {
           float v[BP];
 #pragma unroll
           for (int j = 0; j < BP; ++j) {
-            v[j] = warp_sum(a[0][j] + a[1][j]);
+            const float part = XF == 1
+                                   ? ((j & 1) ? pair_hi(a2[0][j >> 1]) + pair_hi(a2[1][j >> 1])
+                                              : pair_lo(a2[0][j >> 1]) + pair_lo(a2[1][j >> 1]))
+                                   : a[0][j] + a[1][j];
+            v[j] = warp_sum(part);
             a[0][j] = a[1][j] = 0.f;
           }
+#pragma unroll
+          for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
           finish_row_n<BP>(cc.row, v, wr, T, warp, lane, pf, pl, store);
         }
         advance(cc, T);
@@ -246,14 +379,21 @@ __global__ void __launch_bounds__(256) spmm_combine_kernel(const float* __restri
   }
 }
 
-size_t spmm_smem_bytes(int pitch, int nw, int bp) {
-  return (size_t)34 * pitch * bp * 2 + 2 * (size_t)nw * bp * sizeof(float);
+size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf) {
+  return (size_t)34 * pitch * bp * (xf ? 4 : 2) + 2 * (size_t)nw * bp * sizeof(float);
 }
 
 int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8); }
 
-// (warps per block, steps in flight per warp)
-static const int kSpmmVariants[][2] = {{16, 2}, {20, 2}, {12, 3}, {24, 1}};
+// (warps per block, steps in flight per warp, x slot format)
+// fp32 slots (XF 1: packed fp32x2 FMA; XF 2: scalar FMA) measured 1.5-1.7x
+// slower than fp16 slots at batch 4-8 on GB300: every nonzero gathers
+// BP x-values from shared memory per lane, so at batch 8 the gather already
+// needs 16 B per nonzero with fp16 slots and twice that with fp32 slots --
+// shared-memory bandwidth, not FMA issue, is the limit there.  They stay
+// available for tuning; the defaults use fp16 slots.
+static const int kSpmmVariants[][3] = {{16, 2, 0}, {20, 2, 0}, {12, 3, 0}, {24, 1, 0},
+                                       {16, 2, 1}, {16, 2, 2}};
 
 int spmm_variant_count() { return (int)(sizeof(kSpmmVariants) / sizeof(kSpmmVariants[0])); }
 
@@ -261,22 +401,26 @@ int spmm_variant_warps(int variant) {
   return (variant >= 0 && variant < spmm_variant_count()) ? kSpmmVariants[variant][0] : 0;
 }
 
-template <int NW, int U, int BP>
-static cudaError_t launch_spmm_t(const SpmmParams& p, int grid, int flags, cudaStream_t stream) {
-  static int smem_set[64] = {0};
-  auto* k = spmm_kernel<NW, U, BP>;
-  cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(k, grid, NW * 32, spmm_smem_bytes(p.pitch, NW, BP), stream, flags, p);
+int spmm_variant_xf(int variant) {
+  return (variant >= 0 && variant < spmm_variant_count()) ? kSpmmVariants[variant][2] : 0;
 }
 
-template <int NW, int U>
+template <int NW, int U, int BP, int XF>
+static cudaError_t launch_spmm_t(const SpmmParams& p, int grid, int flags, cudaStream_t stream) {
+  static int smem_set[64] = {0};
+  auto* k = spmm_kernel<NW, U, BP, XF>;
+  cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k, grid, NW * 32, spmm_smem_bytes(p.pitch, NW, BP, XF), stream, flags, p);
+}
+
+template <int NW, int U, int XF>
 static cudaError_t launch_spmm_bp(const SpmmParams& p, int bp, int grid, int flags,
                                   cudaStream_t stream) {
   switch (bp) {
-    case 2: return launch_spmm_t<NW, U, 2>(p, grid, flags, stream);
-    case 4: return launch_spmm_t<NW, U, 4>(p, grid, flags, stream);
-    case 8: return launch_spmm_t<NW, U, 8>(p, grid, flags, stream);
+    case 2: return launch_spmm_t<NW, U, 2, XF>(p, grid, flags, stream);
+    case 4: return launch_spmm_t<NW, U, 4, XF>(p, grid, flags, stream);
+    case 8: return launch_spmm_t<NW, U, 8, XF>(p, grid, flags, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -287,10 +431,11 @@ cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
   switch (plan.variant) {
 #define NM_SPMM_CASE(i)                                                                 \
   case i:                                                                              \
-    e = launch_spmm_bp<kSpmmVariants[i][0], kSpmmVariants[i][1]>(p, plan.bp, plan.grid, \
-                                                                  flags, stream);       \
+    e = launch_spmm_bp<kSpmmVariants[i][0], kSpmmVariants[i][1], kSpmmVariants[i][2]>(  \
+        p, plan.bp, plan.grid, flags, stream);                                          \
     break;
-    NM_SPMM_CASE(0) NM_SPMM_CASE(1) NM_SPMM_CASE(2) NM_SPMM_CASE(3)
+    NM_SPMM_CASE(0) NM_SPMM_CASE(1) NM_SPMM_CASE(2) NM_SPMM_CASE(3) NM_SPMM_CASE(4)
+    NM_SPMM_CASE(5)
 #undef NM_SPMM_CASE
     default: return cudaErrorInvalidValue;
   }

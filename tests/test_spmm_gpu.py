@@ -81,10 +81,11 @@ def test_spmm_exact_every_plan(nm, orc, rows, cols):
         ref, _ = oracle_spmm(orc, ov, om, cols, X)
         expect = np.stack([orc.round_f16(r) for r in ref])
         v, m, Xd = to_dev(ov), dev_masks(om), to_dev(X)
-        # the fewest slices whose x tile fits (more are always allowed)
-        ws = nm.nm_spmm_workspace_bytes(rows, cols, batch)
-        s_min = ws // (batch * rows * 4) if ws else 1
+        L = nm.lib()
         for variant in range(nm.nm_spmm_variant_count()):
+            # the fewest slices whose x tile fits this variant (more always may)
+            ws = L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, 0)
+            s_min = ws // (batch * rows * 4) if ws else 1
             for slices in sorted({0, 1, min(2, T), min(3, T), T}):
                 if 0 < slices < s_min:
                     with pytest.raises(nm.NMError) as e:
