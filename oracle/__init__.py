@@ -14,7 +14,8 @@ What the oracle computes (SparseDecoding pages, see ``oracle.c``):
   * ``unpack``      -- the inverse scatter, unselected columns +0.0;
   * ``matvec_f64``  -- y = W x with double accumulation plus s = sum |w||x|;
   * ``spmv_rows_f64`` -- unpack + matvec for chosen rows of a packed matrix;
-  * ``count_bad_words`` -- number of mask words whose popcount is not 16.
+  * ``count_bad_words`` -- number of mask words whose popcount is not 16;
+  * ``silu_mul_f64``  -- the SwiGLU epilogue silu(g) * u of a gate/up pair.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against values fixed independently of this code (numpy's binary16, exact
@@ -67,6 +68,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_spmv_rows_f64.restype = ctypes.c_int
     lib.orc_count_bad_words.argtypes = [_P, _I64, _I64]
     lib.orc_count_bad_words.restype = ctypes.c_int64
+    lib.orc_silu_mul_f64.argtypes = [_P, _P, _I64, _P]
+    lib.orc_silu_mul_f64.restype = ctypes.c_int
     return lib
 
 
@@ -171,6 +174,15 @@ class Oracle:
     def spmv_f64(self, values, masks, cols: int, x):
         rows = np.asarray(masks).shape[0]
         return self.spmv_rows_f64(values, masks, cols, x, np.arange(rows, dtype=np.int64))
+
+    def silu_mul_f64(self, g, u) -> np.ndarray:
+        """h = silu(g) * u in double (the SwiGLU epilogue)."""
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        u = np.ascontiguousarray(u, dtype=np.float64)
+        h = np.zeros_like(g)
+        if self.lib.orc_silu_mul_f64(_ptr(g), _ptr(u), g.size, _ptr(h)) != 0:
+            raise ValueError("orc_silu_mul_f64 rejected its input")
+        return h
 
     def round_f16(self, y) -> np.ndarray:
         """Round doubles to binary16 bit patterns with the oracle's own RNE routine."""

@@ -264,3 +264,19 @@ int64_t orc_count_bad_words(const uint32_t *masks, int64_t rows, int64_t cols)
         if (popcount32(masks[i]) != 16) ++bad;
     return bad;
 }
+
+/* ------------------------------------------------------------------------ */
+/* SwiGLU epilogue of the fused gate+up projection (the decoder layers the    */
+/* pages measure -- Llama-3.1/3.3, Qwen3 -- feed silu(gate) * up into the     */
+/* down projection).                                                         */
+/* ------------------------------------------------------------------------ */
+
+int orc_silu_mul_f64(const double *g, const double *u, int64_t n, double *h)
+{
+    if (!g || !u || !h || n < 0) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) {
+        double silu = g[i] / (1.0 + exp(-g[i]));
+        h[i] = silu * u[i];
+    }
+    return ORC_OK;
+}

@@ -75,6 +75,12 @@ int orc_spmv_rows_f64(const uint16_t *values, const uint32_t *masks,
                       const int64_t *row_ids, int64_t n_ids, double *y,
                       double *s);
 
+/* SwiGLU of a gate/up pair of SpMV outputs, in double:
+ * h[i] = silu(g[i]) * u[i], silu(t) = t / (1 + exp(-t)).  This is the
+ * activation between the fused gate+up projection and the down projection of
+ * the Llama/Qwen decoder layers the pages measure. */
+int orc_silu_mul_f64(const double *g, const double *u, int64_t n, double *h);
+
 /* Number of mask words whose popcount is not 16 (the 50% invariant). */
 int64_t orc_count_bad_words(const uint32_t *masks, int64_t rows, int64_t cols);
 

@@ -356,6 +356,21 @@ def pin_leading_dimension(o, seed=11):
     assert abs(y2[2] - float(ye)) <= 1e-15
 
 
+def pin_silu_mul_closed_forms(o):
+    """silu(t) = t / (1 + e^-t): silu(0) = 0, silu(1) = e / (1 + e),
+    silu(t) - silu(-t) = t (an identity of the logistic function), silu ~ t
+    for large t and ~ 0 for very negative t; h is linear in u."""
+    e = math.e
+    g = np.array([0.0, 1.0, -1.0, 2.5, -2.5, 40.0, -40.0, 0.125])
+    u = np.array([3.0, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0, -2.0])
+    h = o.silu_mul_f64(g, u)
+    assert h[0] == 0.0
+    assert abs(h[1] - e / (1 + e)) <= 1e-15 and abs(h[2] + 1 / (1 + e)) <= 1e-15
+    assert abs((h[3] - h[4]) - 2.5) <= 1e-14
+    assert abs(h[5] - 40.0) <= 1e-12 and abs(h[6]) <= 1e-15
+    assert abs(h[7] - (-2.0) * o.silu_mul_f64([0.125], [1.0])[0]) <= 1e-16
+
+
 ALL_PINS = [
     pin_f16_to_f64_all_patterns,
     pin_f16_from_f64_matches_numpy,
@@ -372,4 +387,5 @@ ALL_PINS = [
     pin_spmv_exact_arithmetic,
     pin_spmv_rows_equals_dense_path,
     pin_leading_dimension,
+    pin_silu_mul_closed_forms,
 ]

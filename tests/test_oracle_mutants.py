@@ -42,6 +42,9 @@ MUTANTS = {
                                  "if (popcount32(masks[i]) > 16) ++bad;"),
     "matvec_ignores_ld": ("dot_row(W + r * ld, x, cols,", "dot_row(W + r * cols, x, cols,"),
     "spmv_rows_ignores_ids": ("int64_t r = row_ids[i];", "int64_t r = i;"),
+    "silu_sign": ("double silu = g[i] / (1.0 + exp(-g[i]));",
+                  "double silu = g[i] / (1.0 + exp(g[i]));"),
+    "silu_mul_drops_up": ("h[i] = silu * u[i];", "h[i] = silu;"),
 }
 
 
