@@ -315,9 +315,11 @@ class Step:
     of `batch` tokens (1: nm_spmv / dense_gemv; 2..8: nm_spmm, and cuBLAS as
     the dense reference since dense_gemv is batch-one)."""
 
-    def __init__(self, nm, mats, layers, device, flags=None, batch=1):
+    def __init__(self, nm, mats, layers, device, flags=None, batch=1, swiglu=False):
         import torch
         self.nm, self.mats, self.layers, self.flags, self.batch = nm, mats, layers, flags, batch
+        # fuse the SwiGLU activation into the gate+up call (batch one only)
+        self.swiglu = [swiglu and batch == 1 and name == "gate_up" for name, _, _ in mats]
         self.x_off, self.y_off = [], []
         xo = yo = 0
         for _, rows, cols in mats:
@@ -353,7 +355,10 @@ class Step:
         return v[0] if self.batch == 1 else v
 
     def call_sparse(self, v, m, l, i):
-        if self.batch == 1:
+        if self.swiglu[i]:
+            y = self.y(l, i)
+            self.nm.nm_spmv_swiglu(v, m, self.x(l, i), h=y[: y.numel() // 2], flags=self.flags)
+        elif self.batch == 1:
             self.nm.nm_spmv(v, m, self.x(l, i), y=self.y(l, i), flags=self.flags)
         else:
             self.nm.nm_spmm(v, m, self.x(l, i), Y=self.y(l, i), workspace=self.ws,
@@ -378,7 +383,9 @@ class Step:
 
     def bytes_sparse(self):
         B = self.batch
-        return self.layers * sum(sparse_bytes(r, c) + (B - 1) * 2 * (r + c) for _, r, c in self.mats)
+        # a fused SwiGLU call writes rows/2 outputs instead of rows
+        return self.layers * sum(sparse_bytes(r, c) + (B - 1) * 2 * (r + c) - (r if f else 0)
+                                 for (_, r, c), f in zip(self.mats, self.swiglu))
 
     def bytes_dense(self):
         B = self.batch
@@ -462,7 +469,7 @@ def run_gpu(args):
     t_setup = time.time()
     dense, xs = make_dense(mats, device, args.batch)
     step = Step(nm, mats, layers, device, flags=None if args.flags < 0 else args.flags,
-                batch=args.batch)
+                batch=args.batch, swiglu=args.swiglu)
     step.fill_x(xs)
     setup_s = time.time() - t_setup
 
@@ -552,6 +559,7 @@ def run_gpu(args):
                           f"{args.slots * step_bytes / layers / 1e9:.1f} GB > L2 (129 MB)"),
             "parallelism": f"replicas x{world}",
             "launch_flags": "library default (programmatic dependent launch)" if args.flags < 0 else args.flags,
+            "gate_up": "nm_spmv_swiglu (SwiGLU fused)" if args.swiglu and args.batch == 1 else "nm_spmv",
         },
         "step_ms": {"median": round(med_ms, 4), "p10": round(float(np.percentile(per, 10)), 4),
                     "p90": round(float(np.percentile(per, 90)), 4)},
@@ -660,6 +668,9 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="llama33_70b_layer")
     ap.add_argument("--pattern", default="2:4")
+    ap.add_argument("--swiglu", action="store_true",
+                    help="run the gate+up projection as nm_spmv_swiglu (SwiGLU fused; "
+                         "rows interleaved gate/up)")
     ap.add_argument("--batch", type=int, default=1,
                     help="tokens per step: 1 = nm_spmv (the headline); 2..8 = nm_spmm, with "
                          "cuBLAS (torch.mm) as the dense reference")

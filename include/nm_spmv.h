@@ -125,6 +125,26 @@ int nm_spmv(const void *values, const uint32_t *masks, int64_t rows, int64_t col
             void *stream);
 
 /* ---------------------------------------------------------------------------
+ * nm_spmv_swiglu -- the gate+up projection of a decoder layer with its SwiGLU
+ * activation fused: h[i] = silu(g_i) * u_i, silu(t) = t / (1 + e^-t), where
+ * g = W_gate x and u = W_up x.  The pages time whole decoding steps of
+ * Llama/Qwen layers (aimodeling.com article, "The Kernel Is the Other Half of
+ * the Answer"), whose gate and up projections feed exactly this product into
+ * the down projection; fusing it saves writing and re-reading both outputs.
+ *   The packed matrix interleaves the two projections: row 2i is gate row i,
+ *   row 2i+1 is up row i (rows = 2 * hidden, even); pack W_gate and W_up
+ *   row-interleaved with nm_pack.
+ *   h : device fp16 [rows / 2], must not overlap the inputs.
+ * g and u are the same fp32 sums nm_spmv would round to fp16; silu and the
+ * product are evaluated in fp32 and h is rounded once to fp16 (RNE).
+ * Other arguments and errors as nm_spmv (rows odd -> NM_ERR_SHAPE).
+ * ------------------------------------------------------------------------- */
+int nm_spmv_swiglu(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                   const void *x, void *h, void *stream);
+int nm_spmv_swiglu_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                      const void *x, void *h, int variant, int grid, int flags, void *stream);
+
+/* ---------------------------------------------------------------------------
  * nm_spmm -- Y = W X for a small batch of tokens (1..8), W in the packed
  * format.  Decoding several tokens at once (small-batch serving, speculative
  * decoding) is the step between the batch-one SpMV and the prefill SpMM the

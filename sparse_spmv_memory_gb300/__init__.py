@@ -27,6 +27,7 @@ __all__ = [
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
     "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
+    "nm_spmv_swiglu",
 ]
 
 NM_OK = 0
@@ -81,6 +82,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "dense_gemv_variant_count": ([], I32),
         "nm_check_masks": ([P, I64, I64, P], I64),
         "nm_check_masks_noalloc": ([P, I64, I64, P], I64),
+        "nm_spmv_swiglu": ([P, P, I64, I64, P, P, P], I32),
+        "nm_spmv_swiglu_ex": ([P, P, I64, I64, P, P, I32, I32, I32, P], I32),
         "nm_spmm_workspace_bytes": ([I64, I64, I32], SZ),
         "nm_spmm_workspace_bytes_ex": ([I64, I64, I32, I32, I32], SZ),
         "nm_spmm": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
@@ -218,6 +221,29 @@ def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int 
                           NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "nm_spmv")
     return y
+
+
+def nm_spmv_swiglu(values, masks, x, h=None, stream=None, variant: int = -1, grid: int = 0,
+                   flags: int | None = None):
+    """h = silu(W_gate x) * (W_up x), the packed matrix holding gate and up rows
+    interleaved (row 2i gate, row 2i+1 up); h fp16 [rows / 2]."""
+    torch = _torch()
+    _need_cuda(values, masks, x)
+    rows = masks.shape[0]
+    cols = x.shape[0]
+    if h is None:
+        h = torch.empty((rows // 2,), dtype=torch.float16, device=x.device)
+    _need_cuda(h)
+    L = lib()
+    if variant < 0 and grid <= 0 and flags is None:
+        st = L.nm_spmv_swiglu(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(h),
+                              _stream(stream))
+    else:
+        st = L.nm_spmv_swiglu_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(h),
+                                 variant, grid, NM_FLAG_PDL if flags is None else flags,
+                                 _stream(stream))
+    _check(st, "nm_spmv_swiglu")
+    return h
 
 
 def nm_spmm_workspace_bytes(rows: int, cols: int, batch: int) -> int:

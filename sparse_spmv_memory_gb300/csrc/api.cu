@@ -296,6 +296,43 @@ int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
+int nm_spmv_swiglu_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                      const void* x, void* h, int variant, int grid, int flags, void* stream) {
+  if (!values || !masks || !x || !h) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || rows % 2 != 0 || cols <= 0 || cols % 32 != 0)
+    return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(x, 16) || !aligned(h, 2))
+    return NM_ERR_ALIGN;
+  const size_t hb = (size_t)rows;  // rows/2 fp16
+  if (overlap(h, hb, values, (size_t)rows * cols) || overlap(h, hb, masks, (size_t)rows * cols / 8) ||
+      overlap(h, hb, x, (size_t)cols * 2))
+    return NM_ERR_ALIAS;
+  if (rows == 0) return NM_OK;
+  SpmvPlan plan;
+  SpmvParams p;
+  int st = make_spmv_plan(rows, cols, variant, grid, &plan, &p);
+  if (st != NM_OK) return st;
+  // blocks own whole (gate, up) pairs; the rows' fp32 sums stay in shared memory
+  if (plan.grid > rows / 2) plan.grid = (int)(rows / 2);
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  const int64_t block_rows_max = 2 * ((rows / 2 + plan.grid - 1) / plan.grid);
+  if (spmv_smem_bytes(p.pitch, plan.warps) + (size_t)block_rows_max * 4 > (size_t)d.smem_optin)
+    return NM_ERR_SHAPE;
+  p.values = static_cast<const uint32_t*>(values);
+  p.masks = masks;
+  p.x = static_cast<const __half*>(x);
+  p.y = static_cast<__half*>(h);
+  p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  cudaError_t e = launch_spmv(p, plan, flags, static_cast<cudaStream_t>(stream), 1);
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmv_swiglu(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                   const void* x, void* h, void* stream) {
+  return nm_spmv_swiglu_ex(values, masks, rows, cols, x, h, -1, 0, NM_FLAG_PDL, stream);
+}
+
 int nm_spmv(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* x,
             void* y, void* workspace, size_t workspace_bytes, void* stream) {
   return nm_spmv_ex(values, masks, rows, cols, x, y, workspace, workspace_bytes, -1, 0,

@@ -30,8 +30,10 @@ struct SpmvPlan {
 int spmv_variant_warps(int variant);
 int spmv_variant_count();
 size_t spmv_smem_bytes(int pitch, int nw);
+// epilogue 0: y = W x; 1: rows are interleaved (gate, up) pairs and y receives
+// h = silu(gate) * up, rows/2 values.
 cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int epilogue = 0);
 
 // ---- dense -----------------------------------------------------------------
 struct GemvParams {

@@ -28,6 +28,13 @@ __device__ __forceinline__ BlockRows block_rows(int64_t rows) {
   return {rows * c / G, rows * (c + 1) / G};
 }
 
+// Pair-aligned variant: rows come in (gate, up) pairs that must stay in one
+// block; the rows/2 pairs are balanced over the blocks.
+__device__ __forceinline__ BlockRows block_row_pairs(int64_t rows) {
+  const int64_t G = gridDim.x, c = blockIdx.x, H = rows / 2;
+  return {2 * (H * c / G), 2 * (H * (c + 1) / G)};
+}
+
 struct WarpRange {
   int64_t sb, se;  // flattened steps [sb, se) of the block
 };

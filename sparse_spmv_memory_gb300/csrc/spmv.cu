@@ -171,17 +171,31 @@ __device__ __forceinline__ void spmv_load(SpmvBatch<U>& bt, SpmvCursor& c, int64
   }
 }
 
-template <int NW, int U, int DEC>
+// Epilogue EPI 1 (SwiGLU): rows are interleaved (gate, up) pairs; each block
+// owns whole pairs, keeps its rows' fp32 sums in shared memory and writes
+// h[i] = silu(gate_i) * up_i (fp16) for its pairs after the cut-row combine.
+template <int NW>
+__device__ __forceinline__ void swiglu_epilogue(const float* ysm, int64_t r0, int64_t r1,
+                                                __half* h) {
+  __syncthreads();
+  for (int64_t k = threadIdx.x; 2 * k < r1 - r0; k += NW * 32) {
+    const float g = ysm[2 * k], u = ysm[2 * k + 1];
+    h[r0 / 2 + k] = __float2half_rn(g / (1.0f + expf(-g)) * u);
+  }
+}
+
+template <int NW, int U, int DEC, int EPI>
 __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;
   float* xs = smem;           // [34][P]
   float* pf = smem + 34 * P;  // [NW] first-row partials
   float* pl = pf + NW;        // [NW] last-row partials
+  float* ysm = pl + NW;       // EPI 1: fp32 sums of the block's rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.steps;
-  const BlockRows br = block_rows(p.rows);
+  const BlockRows br = EPI ? block_row_pairs(p.rows) : block_rows(p.rows);
   const int64_t F = (br.r1 - br.r0) * T;
   const WarpRange wr = warp_range<NW>(F, warp);
 
@@ -197,7 +211,12 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
 
   const uint32_t xs_base = smem_addr(xs);
   const uint32_t row_bytes = 4u * (uint32_t)P;
-  auto store = [&](int64_t row, float v) { p.y[br.r0 + row] = __float2half_rn(v); };
+  auto store = [&](int64_t row, float v) {
+    if (EPI)
+      ysm[row] = v;
+    else
+      p.y[br.r0 + row] = __float2half_rn(v);
+  };
 
   SpmvCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
   float a0 = 0.f, a1 = 0.f;
@@ -229,6 +248,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
 
   __syncthreads();
   combine_cut_rows<NW>(F, T, pf, pl, store);
+  if (EPI) swiglu_epilogue<NW>(ysm, br.r0, br.r1, p.y);
 }
 
 // ---------------------------------------------------------------------------
@@ -250,17 +270,18 @@ __device__ __forceinline__ void load_steps(SpmvBatch<U>& bt, const uint32_t*& vp
   }
 }
 
-template <int NW, int U, int DEC>
+template <int NW, int U, int DEC, int EPI>
 __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;  // == words
   float* xs = smem;
   float* pf = smem + 34 * P;
   float* pl = pf + NW;
+  float* ysm = pl + NW;  // EPI 1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.steps;
-  const BlockRows br = block_rows(p.rows);
+  const BlockRows br = EPI ? block_row_pairs(p.rows) : block_rows(p.rows);
   const int F = (int)((br.r1 - br.r0) * T);
   const WarpRange wr = warp_range<NW>(F, warp);
   const int sb = (int)wr.sb, se = (int)wr.se;
@@ -280,7 +301,12 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
 
   const uint32_t row_bytes = 4u * (uint32_t)P;
   const uint32_t lane_col = smem_addr(xs) + row_bytes + 4u * (uint32_t)lane;
-  auto store = [&](int64_t row, float v) { p.y[br.r0 + row] = __float2half_rn(v); };
+  auto store = [&](int64_t row, float v) {
+    if (EPI)
+      ysm[row] = v;
+    else
+      p.y[br.r0 + row] = __float2half_rn(v);
+  };
 
   int row = sb / T, t = sb - row * T;
   uint32_t col_addr = lane_col + 128u * (uint32_t)t;
@@ -318,27 +344,36 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
 
   __syncthreads();
   combine_cut_rows<NW>(F, T, pf, pl, store);
+  if (EPI) swiglu_epilogue<NW>(ysm, br.r0, br.r1, p.y);
 }
 
 size_t spmv_smem_bytes(int pitch, int nw) {
   return (size_t)(34 * pitch + 2 * nw) * sizeof(float);
 }
 
-template <int NW, int U, int DEC>
-static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, int flags, cudaStream_t stream) {
+template <int NW, int U, int DEC, int EPI>
+static cudaError_t launch_spmv_e(const SpmvParams& p, int grid, int flags, cudaStream_t stream) {
   static int smem_full[64] = {0}, smem_gen[64] = {0};
-  const size_t smem = spmv_smem_bytes(p.pitch, NW);
-  const int64_t block_steps = (p.rows + grid - 1) / grid * p.steps;
+  const int64_t block_rows_max = EPI ? 2 * ((p.rows / 2 + grid - 1) / grid) : 0;
+  const size_t smem = spmv_smem_bytes(p.pitch, NW) + (size_t)block_rows_max * sizeof(float);
+  const int64_t block_steps = ((p.rows + grid - 1) / grid + 2) * p.steps;
   if (p.words % 32 == 0 && block_steps < (int64_t)0x7FFFFFFF) {
-    auto* k = spmv_full_kernel<NW, U, DEC>;
+    auto* k = spmv_full_kernel<NW, U, DEC, EPI>;
     cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_full, 64);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
   }
-  auto* k = spmv_kernel<NW, U, DEC>;
+  auto* k = spmv_kernel<NW, U, DEC, EPI>;
   cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_gen, 64);
   if (e != cudaSuccess) return e;
   return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
+}
+
+template <int NW, int U, int DEC>
+static cudaError_t launch_spmv_t(const SpmvParams& p, int grid, int epi, int flags,
+                                 cudaStream_t stream) {
+  return epi ? launch_spmv_e<NW, U, DEC, 1>(p, grid, flags, stream)
+             : launch_spmv_e<NW, U, DEC, 0>(p, grid, flags, stream);
 }
 
 // (warps per block, steps in flight per warp, decode).  Every variant runs
@@ -358,12 +393,12 @@ int spmv_variant_warps(int variant) {
 }
 
 cudaError_t launch_spmv(const SpmvParams& p, const SpmvPlan& plan, int flags,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int epilogue) {
   switch (plan.variant) {
 #define NM_SPMV_CASE(i)                                                                 \
   case i:                                                                              \
     return launch_spmv_t<kSpmvVariants[i][0], kSpmvVariants[i][1], kSpmvVariants[i][2]>( \
-        p, plan.grid, flags, stream);
+        p, plan.grid, epilogue, flags, stream);
     NM_SPMV_CASE(0) NM_SPMV_CASE(1) NM_SPMV_CASE(2) NM_SPMV_CASE(3) NM_SPMV_CASE(4)
     NM_SPMV_CASE(5) NM_SPMV_CASE(6)
 #undef NM_SPMV_CASE
