@@ -71,13 +71,14 @@ const char *nm_status_string(int status);
 size_t nm_values_bytes(int64_t rows, int64_t cols); /* rows*cols/2 fp16 = rows*cols bytes */
 size_t nm_masks_bytes(int64_t rows, int64_t cols);  /* rows*cols/32 uint32 = rows*cols/8 bytes */
 
-/* Device workspace nm_spmv needs for this shape, in bytes.  The current
- * launch plan reduces every row inside one thread block, so this is 0 for
- * every supported shape; callers may still pass a workspace. */
+/* Device workspace nm_spmv needs for this shape, in bytes: 0 whenever
+ * cols <= nm_spmv_max_cols() (every row is reduced inside one thread block);
+ * longer rows are cut into column slices whose fp32 partial sums go through
+ * the workspace (as nm_spmm with one token).  0 also for invalid shapes. */
 size_t nm_spmv_workspace_bytes(int64_t rows, int64_t cols);
 
-/* Largest cols nm_spmv accepts on the current device (the dense x vector is
- * staged once per thread block in shared memory as fp32). */
+/* Largest cols for which nm_spmv keeps a whole row's x in one block's shared
+ * memory (and needs no workspace) on the current device. */
 int64_t nm_spmv_max_cols(void);
 
 /* ---------------------------------------------------------------------------
@@ -109,8 +110,9 @@ int nm_unpack(const void *values, const uint32_t *masks, int64_t rows, int64_t c
  *   masks     : device uint32 [rows][cols/32], 4-byte aligned.
  *   x         : device fp16 [cols], 16-byte aligned.
  *   y         : device fp16 [rows] (output), must not overlap the inputs.
- *   workspace : device scratch of at least nm_spmv_workspace_bytes(rows,
- *               cols) bytes (may be NULL when that is 0).
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *               nm_spmv_workspace_bytes(rows, cols) bytes (NULL when that is 0,
+ *               i.e. for cols <= nm_spmv_max_cols()).
  * Products and sums are fp32 (fp32 fused multiply-add); y is rounded to fp16
  * with round-to-nearest-even.  The summation order is fixed for a shape and
  * device, so repeated calls give bit-identical y.  Takes no N or M: the
@@ -118,7 +120,9 @@ int nm_unpack(const void *values, const uint32_t *masks, int64_t rows, int64_t c
  * Precondition: every mask word has popcount 16 (nm_pack guarantees it; use
  * nm_check_masks for untrusted data).  A word that breaks it is still read
  * in bounds, but the affected rows are unspecified.
- * cols must be <= nm_spmv_max_cols(); rows == 0 is a no-op.
+ * Rows longer than nm_spmv_max_cols() run column-sliced through the
+ * workspace (still deterministic); an explicit-plan nm_spmv_ex call for such
+ * a shape returns NM_ERR_SHAPE.  rows == 0 is a no-op.
  * ------------------------------------------------------------------------- */
 int nm_spmv(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
             const void *x, void *y, void *workspace, size_t workspace_bytes,

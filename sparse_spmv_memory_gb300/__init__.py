@@ -210,8 +210,12 @@ def nm_spmv(values, masks, x, y=None, workspace=None, stream=None, variant: int 
     if y is None:
         y = torch.empty((rows,), dtype=torch.float16, device=x.device)
     _need_cuda(y, workspace)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     L = lib()
+    if workspace is None and variant < 0:
+        need = L.nm_spmv_workspace_bytes(rows, cols)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if variant < 0 and grid <= 0 and flags is None:
         st = L.nm_spmv(_ptr(values), _ptr(masks), rows, cols, _ptr(x), _ptr(y), _ptr(workspace),
                        ws_bytes, _stream(stream))

@@ -199,6 +199,12 @@ int check_spmv_args(const void* values, const uint32_t* masks, int64_t rows, int
 
 extern "C" {
 
+int64_t nm_spmv_max_cols(void);
+size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant, int slices);
+int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+               const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
+               size_t workspace_bytes, int variant, int grid, int slices, int flags, void* stream);
+
 const char* nm_status_string(int status) {
   switch (status) {
     case NM_OK: return "NM_OK";
@@ -224,9 +230,11 @@ size_t nm_masks_bytes(int64_t rows, int64_t cols) {
 }
 
 size_t nm_spmv_workspace_bytes(int64_t rows, int64_t cols) {
-  (void)rows;
-  (void)cols;
-  return 0;
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return 0;
+  const int64_t max_cols = nm_spmv_max_cols();
+  if (max_cols < 0 || cols <= max_cols) return 0;  // the whole row's x tile fits
+  // longer rows run as a one-token nm_spmm over column slices
+  return nm_spmm_workspace_bytes_ex(rows, cols, 1, -1, 0);
 }
 
 int64_t nm_spmv_max_cols(void) {
@@ -280,9 +288,16 @@ int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
                int grid, int flags, void* stream) {
   int st = check_spmv_args(values, masks, rows, cols, x, y);
   if (st != NM_OK) return st;
-  if (workspace_bytes < nm_spmv_workspace_bytes(rows, cols)) return NM_ERR_WORKSPACE;
-  (void)workspace;
   if (rows == 0) return NM_OK;
+  const int64_t max_cols = nm_spmv_max_cols();
+  if (max_cols > 0 && cols > max_cols && variant < 0) {
+    // a row's x tile does not fit one block: one-token SpMM over column slices,
+    // partial sums through the workspace (nm_spmv_workspace_bytes > 0)
+    return nm_spmm_ex(values, masks, rows, cols, x, cols, 1, y, rows, workspace, workspace_bytes,
+                      -1, grid, 0, flags, stream);
+  }
+  // single-block rows need no workspace; an explicit plan whose x tile does
+  // not fit is refused by make_spmv_plan (NM_ERR_SHAPE)
   SpmvPlan plan;
   SpmvParams p;
   st = make_spmv_plan(rows, cols, variant, grid, &plan, &p);

@@ -231,20 +231,30 @@ def test_pattern_nesting_gives_identical_format_and_output(nm, orc):
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
 
 
-def test_spmv_max_cols(nm, orc):
+def test_spmv_long_rows(nm, orc):
+    """Up to nm_spmv_max_cols() a row's x tile fits one block and no workspace
+    is needed; longer rows run column-sliced through a workspace, and an
+    explicit single-block plan for them is refused."""
     cmax = nm.nm_spmv_max_cols()
     assert cmax >= 28672
     rows = 5
-    W, x = gen(rows, cmax, 10)
-    v, m = nm.nm_pack(to_dev(W), 2, 4)
-    ov, om = orc.prune_pack(W, 2, 4)
-    y_ref, s = orc.spmv_f64(ov, om, cmax, x)
-    assert_within_tol(from_dev(nm.nm_spmv(v, m, to_dev(x))), y_ref, s, "max cols")
-    W2, x2 = gen(rows, cmax + 32, 10)
-    v2, m2 = nm.nm_pack(to_dev(W2), 2, 4)
-    with pytest.raises(nm.NMError) as e:
-        nm.nm_spmv(v2, m2, to_dev(x2))
-    assert e.value.status == 2
+    for cols in (cmax, cmax + 32, 4 * cmax + 1024):
+        W, x = gen(rows, cols, 10)
+        v, m = nm.nm_pack(to_dev(W), 2, 4)
+        ov, om = orc.prune_pack(W, 2, 4)
+        y_ref, s = orc.spmv_f64(ov, om, cols, x)
+        need = nm.nm_spmv_workspace_bytes(rows, cols)
+        assert (need == 0) == (cols <= cmax)
+        assert_within_tol(from_dev(nm.nm_spmv(v, m, to_dev(x))), y_ref, s, f"cols {cols}")
+        if need:
+            L = nm.lib()
+            y = torch.empty(rows, dtype=torch.float16, device="cuda")
+            st_ = torch.cuda.current_stream().cuda_stream
+            xd = to_dev(x)
+            assert L.nm_spmv(v.data_ptr(), m.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr(),
+                             None, 0, st_) == 5          # workspace required
+            assert L.nm_spmv_ex(v.data_ptr(), m.data_ptr(), rows, cols, xd.data_ptr(),
+                                y.data_ptr(), None, 0, 0, 0, 1, st_) == 2   # single-block plan
 
 
 def test_corrupt_masks_stay_in_bounds(nm, orc):
