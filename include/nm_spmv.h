@@ -117,6 +117,10 @@ int nm_unpack(const void *values, const uint32_t *masks, int64_t rows, int64_t c
  * with round-to-nearest-even.  The summation order is fixed for a shape and
  * device, so repeated calls give bit-identical y.  Takes no N or M: the
  * packed format is the same for all four patterns.
+ * Pruned weights are structural zeros and are never multiplied: a
+ * non-finite x[c] reaches only the rows that keep column c (where IEEE rules
+ * apply: inf * w = +-inf, NaN propagates, +inf + -inf = NaN); every other row
+ * is what it would be with x[c] = 0.
  * Precondition: every mask word has popcount 16 (nm_pack guarantees it; use
  * nm_check_masks for untrusted data).  A word that breaks it is still read
  * in bounds, but the affected rows are unspecified.
@@ -161,7 +165,8 @@ int nm_spmv_swiglu_ex(const void *values, const uint32_t *masks, int64_t rows, i
  *       nm_spmm_workspace_bytes(rows, cols, batch) bytes (0 when a whole row's
  *       x tile fits in one block's shared memory, else fp32 partial sums of
  *       column slices).  May be NULL when that is 0.
- * Same arithmetic, rounding and determinism as nm_spmv; each column of Y is
+ * Same arithmetic, rounding, determinism and structural-zero rule as nm_spmv
+ * (a non-finite activation of token j reaches only column j of Y); each column of Y is
  * within the same tolerance of the exact product (and equals nm_spmv's
  * result whenever the sums are exact).  batch outside 1..8 -> NM_ERR_SHAPE;
  * a short workspace -> NM_ERR_WORKSPACE.  Y must not overlap any input or the

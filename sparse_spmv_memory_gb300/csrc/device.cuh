@@ -41,13 +41,6 @@ __device__ __forceinline__ uint4 ld_keep_v4(const void* p) {
   return v;
 }
 
-// Fire-and-forget prefetch of a contiguous global range into L2 (the address
-// must be 16-byte aligned and the size a multiple of 16).  It keeps many more
-// bytes in flight than the registers of the consuming loads could.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Mask of the b low bits, (1 << b) - 1; b >= 32 (and ~0u) gives all ones.
 __device__ __forceinline__ uint32_t low_bits(uint32_t b) {
   uint32_t r;

@@ -21,7 +21,8 @@
 //    warp's steps are one contiguous stretch of memory walked by pointer
 //    increments with no per-lane predication; spmv_kernel for any other cols
 //    (ragged last step, lanes past the row end load nothing).
-//  * x is staged once per block in shared memory as fp32, TRANSPOSED:
+//  * x is staged once per block in shared memory, one 32-bit slot per column
+//    (fp32, or the fp16 bits in the slot's low half), TRANSPOSED:
 //    xs[b][w] = x[32*w + b].  Lanes of a warp always work on 32 consecutive
 //    words, so whatever bit b each lane is at, the 32 reads fall in 32
 //    distinct banks: the gather never has a bank conflict, for any pattern.
@@ -34,6 +35,11 @@
 //    read stays inside the tile without a branch.  fp32 FMA (or, with x kept as
 //    fp16, one mixed fp16*fp16+fp32 FMA), warp butterfly, and rows cut between
 //    warps summed in warp order (deterministic).
+//  * Programmatic dependent launch (NM_FLAG_PDL): a block signals its
+//    dependents as soon as it starts and waits for the previous kernel on the
+//    stream only before it reads x or writes y, so in a chain of projections
+//    the next launch ramps up under the tail of the current one.  With
+//    NM_FLAG_WEIGHTS_CONST the first weight loads are issued before that wait.
 //  * No tensor cores: batch-one SpMV does ~0.9 flop per byte, far below the
 //    tensor roofline; the bound is HBM bandwidth.
 #include <cuda_fp16.h>
