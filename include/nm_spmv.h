@@ -242,6 +242,44 @@ int dense_gemv_ex(const void *W, int64_t rows, int64_t cols, int64_t ld,
 int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * nm_spmm_prefill -- Y = W X for a prefill-sized batch of T tokens (any
+ * T >= 1; meant for T beyond the 1..8 of nm_spmm), W in the packed format, on
+ * the tensor cores.  Prefill is the compute-bound regime the pages set
+ * against batch-one decoding (aimodeling.com article, "The Kernel Is the
+ * Other Half of the Answer"; news.bitwarelabs.com summary, "What's new"):
+ * each block expands a 128-row tile of W from values + masks into dense fp16
+ * in shared memory and multiplies it with up to 512 tokens of X by
+ * tcgen05.mma (fp16 x fp16 products, fp32 accumulation in tensor memory).
+ *   X : device fp16 [T][ldx], 16-byte aligned, ldx % 8 == 0, ldx >= cols;
+ *       token t's activations are X[t][0..cols).
+ *   Y : device fp16 [T][ldy] (output), ldy >= rows; Y[t][r] = sum_c W[r][c] X[t][c],
+ *       rounded once to fp16 (round-to-nearest-even).
+ *   values / masks : as for nm_spmv (values 32-byte aligned).
+ * Pruned weights enter the products as +0 (so, unlike nm_spmv, a non-finite
+ * X[t][c] also turns the rows that do not keep column c into NaN).  The
+ * tensor core's summation order is fixed, so repeated calls give identical
+ * bits; each element is within the nm_spmv tolerance of the exact product.
+ * Limits: rows < 2^31 and ceil(rows / 128) <= 65535; T < 2^31.  T == 0 or
+ * rows == 0 is a no-op.  Y must not overlap any input.  No workspace.
+ * nm_spmm_prefill_ex takes a kernel variant (< 0: chosen from T;
+ * 0..nm_spmm_prefill_variant_count()-1: 512 tokens per block with 4 pipeline
+ * stages, 256, 128, 64 tokens, and 512 tokens with 5 stages).
+ * ------------------------------------------------------------------------- */
+int nm_spmm_prefill(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                    const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, void *stream);
+int nm_spmm_prefill_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                       const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, int variant,
+                       void *stream);
+int nm_spmm_prefill_variant_count(void);
+
+/* nm_wait_timeouts -- how many times a tensor-core kernel's bounded wait on
+ * one of its own barriers gave up (each such wait ends after 2 s, after which
+ * the kernel abandons its work, skips its stores and returns, rather than
+ * hang).  Zero in every correct run; reset to zero when `reset` != 0.
+ * Host-synchronous (reads a device counter); negative nm_status on error. */
+int64_t nm_wait_timeouts(int reset);
+
+/* ---------------------------------------------------------------------------
  * nm_check_masks_noalloc -- the same count as nm_check_masks, without any
  * device allocation.  The paper has no counterpart to this entry point; it
  * exists for callers that must not allocate device memory while they run --

@@ -27,7 +27,7 @@ __all__ = [
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
     "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
-    "nm_spmv_swiglu",
+    "nm_spmv_swiglu", "nm_spmm_prefill", "nm_spmm_prefill_variant_count", "nm_wait_timeouts",
 ]
 
 NM_OK = 0
@@ -89,6 +89,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_spmm": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
         "nm_spmm_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, I32, P], I32),
         "nm_spmm_variant_count": ([], I32),
+        "nm_spmm_prefill": ([P, P, I64, I64, P, I64, I64, P, I64, P], I32),
+        "nm_spmm_prefill_ex": ([P, P, I64, I64, P, I64, I64, P, I64, I32, P], I32),
+        "nm_spmm_prefill_variant_count": ([], I32),
+        "nm_wait_timeouts": ([I32], I64),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -289,6 +293,43 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
                           NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "nm_spmm")
     return Y
+
+
+def nm_spmm_prefill_variant_count() -> int:
+    return lib().nm_spmm_prefill_variant_count()
+
+
+def nm_spmm_prefill(values, masks, X, Y=None, stream=None, variant: int = -1,
+                    cols: int | None = None):
+    """Y = W X for a prefill-sized batch on the tensor cores: X fp16 [T][ldx]
+    (first ``cols`` columns used), Y fp16 [T][ldy]."""
+    torch = _torch()
+    _need_cuda(values, masks, X)
+    rows = masks.shape[0]
+    T, ldx = X.shape
+    cols = ldx if cols is None else cols
+    if X.stride(1) != 1 or (Y is not None and Y.stride(1) != 1):
+        raise ValueError("X and Y must have unit column stride")
+    if Y is None:
+        Y = torch.empty((T, rows), dtype=torch.float16, device=X.device)
+    _need_cuda(Y)
+    L = lib()
+    if variant < 0:
+        st = L.nm_spmm_prefill(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), T,
+                               _ptr(Y), Y.stride(0), _stream(stream))
+    else:
+        st = L.nm_spmm_prefill_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), T,
+                                  _ptr(Y), Y.stride(0), variant, _stream(stream))
+    _check(st, "nm_spmm_prefill")
+    return Y
+
+
+def nm_wait_timeouts(reset: bool = False) -> int:
+    """How many bounded in-kernel waits gave up (0 in every correct run)."""
+    r = lib().nm_wait_timeouts(1 if reset else 0)
+    if r < 0:
+        raise NMError(-r, "nm_wait_timeouts")
+    return r
 
 
 def dense_gemv(W, x, y=None, cols: int | None = None, stream=None, variant: int = -1,

@@ -460,6 +460,50 @@ int nm_spmm(const void* values, const uint32_t* masks, int64_t rows, int64_t col
                     -1, 0, 0, NM_FLAG_PDL, stream);
 }
 
+int nm_spmm_prefill_variant_count(void) { return spmm_tc_variant_count(); }
+
+int nm_spmm_prefill_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                       const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, int variant,
+                       void* stream) {
+  if (!values || !masks || !X || !Y) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || (rows + 127) / 128 > 65535 || cols <= 0 || cols % 32 != 0 ||
+      T < 0 || T >= kMaxRows || ldx < cols || ldy < rows)
+    return NM_ERR_SHAPE;
+  if (variant >= spmm_tc_variant_count()) return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
+      !aligned(Y, 2))
+    return NM_ERR_ALIGN;
+  if (rows == 0 || T == 0) return NM_OK;
+  const size_t yb = (size_t)((T - 1) * ldy + rows) * 2;
+  const size_t xb = (size_t)((T - 1) * ldx + cols) * 2;
+  if (overlap(Y, yb, values, (size_t)rows * cols) || overlap(Y, yb, masks, (size_t)rows * cols / 8) ||
+      overlap(Y, yb, X, xb))
+    return NM_ERR_ALIAS;
+  SpmmTcParams p;
+  p.values = values;
+  p.masks = masks;
+  p.X = X;
+  p.ldx = ldx;
+  p.Y = static_cast<__half*>(Y);
+  p.ldy = ldy;
+  p.rows = rows;
+  p.words = (int)(cols / 32);
+  p.T = T;
+  if (variant < 0) variant = spmm_tc_default_variant(T);
+  cudaError_t e = launch_spmm_tc(p, variant, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmm_prefill(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                    const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, void* stream) {
+  return nm_spmm_prefill_ex(values, masks, rows, cols, X, ldx, T, Y, ldy, -1, stream);
+}
+
+int64_t nm_wait_timeouts(int reset) {
+  unsigned long long n = 0;
+  return read_wait_timeouts(&n, reset) == cudaSuccess ? (int64_t)n : -NM_ERR_CUDA;
+}
+
 int64_t nm_check_masks(const uint32_t* masks, int64_t rows, int64_t cols, void* stream) {
   if (!masks) return -NM_ERR_NULL;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return -NM_ERR_SHAPE;

@@ -93,6 +93,26 @@ size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf);
 cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
                         cudaStream_t stream);
 
+// ---- prefill-sized batches on the tensor cores -------------------------------
+struct SpmmTcParams {
+  const void* values;       // fp16 [rows][words*16], 16-byte aligned
+  const uint32_t* masks;    // [rows][words]
+  const void* X;            // fp16 [T][ldx], 16-byte aligned, ldx % 8 == 0
+  int64_t ldx;
+  __half* Y;                // fp16 [T][ldy]
+  int64_t ldy;
+  int64_t rows;
+  int words;                // cols / 32
+  int64_t T;                // tokens
+};
+
+int spmm_tc_variant_count();
+int spmm_tc_default_variant(int64_t T);
+int spmm_tc_block_tokens(int variant);
+cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream);
+// Number of bounded mbarrier waits that gave up since the last reset.
+cudaError_t read_wait_timeouts(unsigned long long* count, int reset);
+
 // ---- format ----------------------------------------------------------------
 cudaError_t launch_pack(const __half* W, int64_t rows, int64_t cols, int64_t ld, int M,
                         __half* values, uint32_t* masks, cudaStream_t stream);

@@ -1,0 +1,406 @@
+// prefill.cu -- Y = W X for a prefill-sized batch of tokens, W in the N:M
+// bitmask format (compact fp16 values + one 32-bit mask word per 32 input
+// columns), on the sm_103a tensor cores.
+//
+// The operation is the pages' SpMM regime (aimodeling.com article, "The
+// Kernel Is the Other Half of the Answer", and news.bitwarelabs.com summary,
+// "What's new": prefill is compute-bound, decode is bandwidth-bound).  The
+// packed format is the same one nm_spmv streams, so a model keeps one copy of
+// its weights for both regimes.
+//
+// Design (this library's own; the pages give no prefill kernel):
+//  * A block owns a tile of BM = 128 rows of W and BN = NB * NMMA tokens; its
+//    fp32 accumulator D (128 x BN) lives in tensor memory, row m in TMEM lane
+//    m.  K advances one mask word (32 columns) per pipeline stage.
+//  * Warp 0 (producer): per stage, a TMA load of the token tile of X
+//    (BN x 32 fp16, 64-byte swizzle) and of the tile's compact values
+//    (128 rows x 16 fp16), plus a 4-byte cp.async of each row's mask word;
+//    all complete on the stage's "full" mbarrier.
+//  * Warps 2..9 (densify): expand each row's 16 kept values into the 32
+//    columns of a K-major, 64-byte-swizzled fp16 tile in shared memory, the
+//    layout the MMA descriptor names.  A lane builds two adjacent columns:
+//    the rank of its first column among the word's set bits (one popc) is the
+//    index of its value in the compact row; absent columns become +0.
+//  * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (M = 128,
+//    N = NMMA, K = 16; two per stage and N-part) on the densified tile and the
+//    X tile, and tcgen05.commit frees the stage when those MMAs are done.
+//  * Epilogue (warps 2..9): tcgen05.ld of the accumulator, fp32 -> fp16 RNE,
+//    stores to Y[t][r].
+//  * Every mbarrier wait gives up after kWaitLimitNs (counted in
+//    g_wait_timeouts); the roles then skip to teardown, which waits for the
+//    copies and MMAs already issued before tensor memory is freed.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "device.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace nmk {
+namespace tc {
+
+constexpr int BM = 128;                // rows of W per block = TMEM lanes
+constexpr int BK = 32;                 // K columns per stage = one mask word
+constexpr int ROW_BYTES = BK * 2;      // 64-byte rows of the swizzled tiles
+constexpr int A_BYTES = BM * ROW_BYTES;  // densified W tile
+constexpr int V_BYTES = BM * 32;       // compact values: 16 fp16 per row
+constexpr int M_BYTES = BM * 4;        // one mask word per row (cp.async ring)
+constexpr int MW = 4;                  // mask words per TMA box (16 bytes per row)
+constexpr int MT_SLOT = BM * MW * 4;   // 2 KiB: the masks of MW consecutive stages
+constexpr int DENSIFY_WARPS = 8;
+constexpr int THREADS = (2 + DENSIFY_WARPS) * 32;
+constexpr int ROWS_PER_WARP = BM / DENSIFY_WARPS;  // 16: two rows per pass
+
+constexpr uint32_t tmem_cols_for(int n) {
+  return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
+}
+
+// MT: masks arrive by TMA, MW stages' worth per box, into MT_SLOTS slots
+// (needs the row pitch of the mask array, words * 4 bytes, to be a multiple
+// of 16); otherwise by 4-byte cp.async into a per-stage ring.  A slot is
+// refilled at stage kt + MW * MT_SLOTS; the producer issues that stage only
+// after the MMA (hence the densify) of stage kt + MW * MT_SLOTS - STAGES is
+// done, which is at or after the slot's last reader kt + MW - 1 when
+// MW * MT_SLOTS >= STAGES + MW - 1.
+template <int NMMA, int NB, int STAGES, bool MT>
+struct Layout {
+  static constexpr int BN = NMMA * NB;
+  static constexpr int B_BYTES = BN * ROW_BYTES;
+  static constexpr int A_OFF = 0;
+  static constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
+  static constexpr int V_OFF = B_OFF + STAGES * B_BYTES;
+  static constexpr int M_OFF = V_OFF + STAGES * V_BYTES;
+  static constexpr int MT_SLOTS = (STAGES + MW - 1 + MW - 1) / MW;
+  static constexpr int M_REGION = MT ? MT_SLOTS * MT_SLOT : STAGES * M_BYTES;
+  static constexpr int BAR_OFF = M_OFF + M_REGION;  // full, empty, afull, accum
+  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1) * 8;
+  static constexpr int BYTES = SLOT_OFF + 16;
+  static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
+  static constexpr uint32_t TX_BYTES = V_BYTES + B_BYTES;  // + MT_SLOT when masks load
+  static_assert(!MT || MW * MT_SLOTS >= STAGES + MW - 1, "mask slot reused too early");
+  static_assert(NMMA % 16 == 0 && NMMA >= 16 && NMMA <= 256, "tcgen05 M=128 needs N in 16..256");
+  static_assert(BN >= 64 && BN <= 512, "epilogue splits BN over two warps of 32 columns");
+  static_assert(B_OFF % 1024 == 0 && (NMMA * ROW_BYTES) % 1024 == 0, "swizzled tiles 1024-aligned");
+};
+
+// 128 rows x 32 columns: lane (h, p) builds columns 2p, 2p+1 of rows
+// r_i = dw * 16 + 2 i + h, i = 0..7.  The shared-memory accesses are issued
+// in three batches (8 mask words, 16 values, 8 stores) so that each batch's
+// latency is paid once per stage rather than once per row.
+// sMw: this stage's mask word of row 0; mstride: bytes from one row's word
+// to the next row's.
+__device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t sMw,
+                                              uint32_t mstride, int dw, int lane) {
+  constexpr int R = ROWS_PER_WARP / 2;
+  const int h = lane >> 4, p = lane & 15;
+  const uint32_t b0 = 2u * p;
+  const uint32_t below = (1u << b0) - 1u;       // columns of the word left of 2p
+  const uint32_t col_byte = (uint32_t)(p & 3) * 4u;
+  const uint32_t chunk = (uint32_t)(p >> 2);
+  const uint32_t r_first = (uint32_t)(dw * ROWS_PER_WARP + h);
+  uint32_t m[R], q[R], v0[R], v1[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) m[i] = lds_u32(sMw + mstride * (r_first + 2 * i));
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const uint32_t r = r_first + 2 * i;
+    const uint32_t c = __popc(m[i] & below);     // rank of column 2p among kept columns
+    q[i] = (m[i] >> b0) & 3u;                    // bit 0: column 2p kept, bit 1: 2p+1 kept
+    const uint32_t a0 = sV + 32u * r + 2u * c;
+    v0[i] = lds_u16_32(a0);
+    v1[i] = lds_u16_32(a0 + ((q[i] & 1u) << 1));
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const uint32_t r = r_first + 2 * i;
+    // byte k of keep = 0xFF when its column is kept: sign-replicate bytes 0/1
+    // of q * 0x4080 (bit 7 <- column 2p, bit 15 <- column 2p+1).
+    const uint32_t keep = prmt(q[i] * 0x4080u, 0u, 0x9988u);
+    const uint32_t out = prmt(v0[i], v1[i], 0x5410u) & keep;
+    // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3, and
+    // (r >> 1) & 3 == i & 3 because dw * 16 is a multiple of 8.
+    const uint32_t phys = r * ROW_BYTES + ((chunk ^ (uint32_t)(i & 3)) << 4) + col_byte;
+    sts_u32(sA + phys, out);
+  }
+}
+
+template <int NMMA, int NB, int STAGES, bool MT>
+__global__ void __launch_bounds__(THREADS, 1)
+    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
+                   const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
+                   __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy) {
+  using L = Layout<NMMA, NB, STAGES, MT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sA = base + L::A_OFF, sB = base + L::B_OFF, sV = base + L::V_OFF,
+                 sM = base + L::M_OFF, bars = base + L::BAR_OFF, slot = base + L::SLOT_OFF;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (STAGES + s); };
+  auto afull = [&](int s) { return bars + 8u * (2 * STAGES + s); };
+  const uint32_t accum = bars + 8u * (3 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = (int64_t)blockIdx.y * BM;
+  const int64_t n0 = (int64_t)blockIdx.x * L::BN;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), MT ? 1 : 1 + 32);    // expect_tx arrival (+ 32 cp.async arrivals)
+      mbar_init(empty(s), 1);                 // tcgen05.commit
+      mbar_init(afull(s), DENSIFY_WARPS);     // one arrival per densify warp
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_x);
+    if (MT) prefetch_tmap(&tm_m);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  uint32_t tmem_base;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(slot) : "memory");
+
+  if (warp == 0) {
+    // ---- producer ------------------------------------------------------
+    int issued = 0;
+    for (int kt = 0; kt < words; ++kt) {
+      const int s = kt % STAGES, u = kt / STAGES;
+      int ok = 1;
+      if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      if (lane == 0) {
+        const bool mask_load = MT && kt % MW == 0;
+        mbar_arrive_expect_tx(full(s), L::TX_BYTES + (mask_load ? MT_SLOT : 0));
+        if (mask_load)
+          tma_load_2d(sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT, &tm_m, kt, (int)r0, full(s));
+        tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          tma_load_2d(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES, &tm_x, kt * BK,
+                      (int)(n0 + j * NMMA), full(s));
+      }
+      if (!MT) {
+#pragma unroll
+        for (int i = 0; i < BM / 32; ++i) {
+          const int rr = lane + 32 * i;
+          const int64_t gr = r0 + rr;
+          const bool in = gr < rows;
+          cp_async_4(sM + s * M_BYTES + 4u * rr, masks + (in ? gr : 0) * words + kt, in ? 4u : 0u);
+        }
+        cp_async_arrive_noinc(full(s));
+      }
+      issued = kt + 1;
+    }
+    cp_async_wait_all();
+    // Teardown must not free shared memory under copies still in flight: wait
+    // (bounded) for the last stages this warp issued.
+    if (lane == 0) {
+      const int first = issued > STAGES ? issued - STAGES : 0;
+      for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer ----------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
+      for (int kt = 0; kt < words; ++kt) {
+        const int s = kt % STAGES, u = kt / STAGES;
+        if (!mbar_wait(full(s), u & 1)) break;
+        if (!mbar_wait(afull(s), u & 1)) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+          const uint64_t ad = smem_desc_sw64(sA + s * A_BYTES + ks * 32);
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            const uint64_t bd = smem_desc_sw64(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES + ks * 32);
+            mma_f16(tmem_base + (uint32_t)(j * NMMA), ad, bd, idesc, (kt | ks) != 0);
+          }
+        }
+        mma_commit(empty(s));
+      }
+      mma_commit(accum);  // also after an early exit: completes once issued MMAs finish
+    }
+    __syncwarp();
+  } else {
+    // ---- densify, then epilogue -----------------------------------------
+    const int dw = warp - 2;
+    bool ok = true;
+    for (int kt = 0; kt < words; ++kt) {
+      const int s = kt % STAGES, u = kt / STAGES;
+      // The warp decides together, so no lane is left behind at a warp barrier.
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full(s), u & 1))) { ok = false; break; }
+      // With MT the stage's masks came with stage MW * (kt / MW), whose full
+      // barrier this warp has already seen complete (stages are consumed in order).
+      const uint32_t sMw = MT ? sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT + (kt % MW) * 4u
+                              : sM + s * M_BYTES;
+      densify_stage(sA + s * A_BYTES, sV + s * V_BYTES, sMw, MT ? MW * 4u : 4u, dw, lane);
+      // Each lane orders its tile writes before the tensor core's reads; the
+      // warp barrier then lets one release-arrive publish all 32 lanes' writes
+      // (one arrival per warp: 32 arrivals on one barrier word serialise).
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull(s));
+    }
+    if (!mbar_wait(accum, 0)) ok = false;
+    tc_fence_after_sync();
+    // tcgen05.ld is a warp-wide instruction: the whole warp reads or none does.
+    if (__all_sync(0xFFFFFFFFu, ok)) {
+      const int quad = warp & 3;              // TMEM lanes 32*quad .. +31
+      const int half = dw >> 2;               // which half of the BN columns
+      const int64_t r = r0 + 32 * quad + lane;
+      const bool row_ok = r < rows;
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * quad) << 16);
+#pragma unroll 1
+      for (int c0 = half * (L::BN / 2); c0 < (half + 1) * (L::BN / 2); c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32(tbase + (uint32_t)c0, v);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int64_t t = n0 + c0 + i;
+            if (t < T) Y[t * ldy + r] = __float2half_rn(__uint_as_float(v[i]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ---- host ------------------------------------------------------------------
+struct Variant {
+  int nmma, nb, stages;
+};
+constexpr Variant kVariants[] = {{256, 2, 4}, {256, 1, 6}, {128, 1, 8}, {64, 1, 8}, {256, 2, 5}};
+constexpr int kVariantCount = sizeof(kVariants) / sizeof(kVariants[0]);
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiled encode_fn() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+                      uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swz,
+                      CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NMMA, int NB, int STAGES, bool MT>
+static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
+  using L = Layout<NMMA, NB, STAGES, MT>;
+  CUtensorMap tm_v, tm_x, tm_m;
+  memset(&tm_m, 0, sizeof(tm_m));
+  if (MT && !encode_2d(&tm_m, p.masks, (uint64_t)p.words, (uint64_t)p.rows,
+                       (uint64_t)p.words * 4, MW, BM, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT32))
+    return cudaErrorInvalidValue;
+  if (!encode_2d(&tm_v, p.values, (uint64_t)p.words * 16, (uint64_t)p.rows,
+                 (uint64_t)p.words * 32, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tm_x, p.X, (uint64_t)p.words * 32, (uint64_t)p.T, (uint64_t)p.ldx * 2, BK,
+                 NMMA, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, MT>;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+  }
+  const dim3 grid((unsigned)((p.T + L::BN - 1) / L::BN), (unsigned)((p.rows + BM - 1) / BM));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, k, tm_v, tm_x, tm_m, p.masks, p.Y, p.rows, p.words, p.T,
+                            p.ldy);
+}
+
+// Mask words by TMA when the mask array allows it (16-byte aligned, row pitch
+// words * 4 a multiple of 16: every decoder shape), else by cp.async.
+template <int NMMA, int NB, int STAGES>
+static cudaError_t launch_tc(const SpmmTcParams& p, cudaStream_t stream) {
+  const bool mt = p.words % 4 == 0 && (reinterpret_cast<uintptr_t>(p.masks) & 15) == 0;
+  return mt ? launch_tc_mt<NMMA, NB, STAGES, true>(p, stream)
+            : launch_tc_mt<NMMA, NB, STAGES, false>(p, stream);
+}
+
+}  // namespace tc
+
+int spmm_tc_variant_count() { return tc::kVariantCount; }
+
+// Measured on GB300 (70B- and 8B-shaped decoder matrices): 512 tokens per
+// block with 5 stages is fastest from T = 512 up; at T = 256 one 256-token
+// N-part; below, the 128- and 64-token blocks waste the least of the MMA.
+int spmm_tc_default_variant(int64_t T) {
+  if (T > 256) return 4;
+  if (T > 128) return 1;
+  if (T > 64) return 2;
+  return 3;
+}
+
+int spmm_tc_block_tokens(int variant) {
+  return tc::kVariants[variant].nmma * tc::kVariants[variant].nb;
+}
+
+cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
+  switch (variant) {
+    case 0: return tc::launch_tc<256, 2, 4>(p, stream);
+    case 1: return tc::launch_tc<256, 1, 6>(p, stream);
+    case 2: return tc::launch_tc<128, 1, 8>(p, stream);
+    case 3: return tc::launch_tc<64, 1, 8>(p, stream);
+    case 4: return tc::launch_tc<256, 2, 5>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t read_wait_timeouts(unsigned long long* count, int reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));
+  if (e != cudaSuccess || !reset) return e;
+  const unsigned long long zero = 0;
+  return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+}
+
+}  // namespace nmk

@@ -1,0 +1,164 @@
+"""GPU parity of the tensor-core prefill SpMM (nm_spmm_prefill: Y = W X for
+T tokens) against the CPU oracle.  Every column of Y is an SpMV, so the
+oracle's packed SpMV of each token is the reference.  Bit for bit on
+exact-arithmetic inputs (every product and partial sum is a multiple of 2^-6
+below 2^12, exact in the fp32 accumulator whatever the order) for every
+kernel variant, on shapes with ragged row and token tails; within the SpMV
+tolerance on random inputs for all four patterns; full-size decoder shapes
+on sampled rows and tokens."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import PATTERNS, f16_to_f64, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def nm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_spmv_memory_gb300 import _build
+    _build.build()
+    import sparse_spmv_memory_gb300 as m
+    m.lib()
+    m.nm_wait_timeouts(reset=True)
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.Oracle()
+
+
+def gen(rows, cols, T, tag, exact=False):
+    sw = synth.stream_id(70, tag, rows, cols, T, 0)
+    sx = synth.stream_id(70, tag, rows, cols, T, 1)
+    if exact:
+        W = synth.int_f16((rows, cols), 0, sw, -8, 8, -6)
+        X = synth.int_f16((T, cols), 0, sx, -2, 2, 0)
+    else:
+        W = synth.weights(rows, cols, 0, sw)
+        X = synth.normal_f16((T, cols), 0, sx, synth.X_SIGMA)
+    return W, X
+
+
+def oracle_Y(orc, ov, om, cols, X):
+    ys, ss = [], []
+    for t in range(X.shape[0]):
+        y, s = orc.spmv_f64(ov, om, cols, X[t])
+        ys.append(y)
+        ss.append(s)
+    return np.stack(ys), np.stack(ss)
+
+
+def dev_packed(orc, W, N, M):
+    ov, om = orc.prune_pack(W, N, M)
+    v = to_dev(ov)
+    m = torch.from_numpy(om.view(np.int32)).cuda()
+    return ov, om, v, m
+
+
+EXACT_SHAPES = [(128, 32, 64), (300, 1056, 77), (257, 2048, 600), (1000, 1024, 513),
+                (64, 4096, 9)]
+
+
+@pytest.mark.parametrize("rows,cols,T", EXACT_SHAPES)
+def test_prefill_exact_every_variant(nm, orc, rows, cols, T):
+    W, X = gen(rows, cols, T, 1, exact=True)
+    ov, om, v, m = dev_packed(orc, W, 2, 4)
+    y_ref, _ = oracle_Y(orc, ov, om, cols, X)
+    want = orc.round_f16(y_ref).reshape(y_ref.shape)
+    Xd = to_dev(X)
+    for variant in range(nm.nm_spmm_prefill_variant_count()):
+        Y = from_dev(nm.nm_spmm_prefill(v, m, Xd, variant=variant))
+        bad = np.argwhere(Y != want)
+        assert bad.size == 0, f"variant {variant}: {len(bad)} mismatches, first (t, r) {bad[:4].tolist()}"
+    assert nm.nm_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("N,M", PATTERNS)
+def test_prefill_within_tolerance(nm, orc, N, M):
+    rows, cols, T = 640, 4096, 300
+    W, X = gen(rows, cols, T, 2 + N)
+    ov, om, v, m = dev_packed(orc, W, N, M)
+    y_ref, s = oracle_Y(orc, ov, om, cols, X)
+    Y = f16_to_f64(from_dev(nm.nm_spmm_prefill(v, m, to_dev(X))))
+    err = np.abs(Y - y_ref)
+    assert np.all(err <= oracle.tolerance(s)), float((err / oracle.tolerance(s)).max())
+    assert nm.nm_wait_timeouts() == 0
+
+
+def test_prefill_strided_and_deterministic(nm, orc):
+    """X and Y with leading dimensions wider than cols / rows: only the
+    addressed elements are read and written, and repeated calls agree."""
+    rows, cols, T = 200, 2048, 130
+    W, X = gen(rows, cols, T, 9, exact=True)
+    ov, om, v, m = dev_packed(orc, W, 4, 8)
+    y_ref, _ = oracle_Y(orc, ov, om, cols, X)
+    Xw = torch.zeros((T, cols + 64), dtype=torch.float16, device="cuda")
+    Xw[:, :cols] = to_dev(X)
+    Yw = torch.full((T, rows + 40), -7.0, dtype=torch.float16, device="cuda")
+    nm.nm_spmm_prefill(v, m, Xw, Y=Yw, cols=cols)
+    got = from_dev(Yw[:, :rows].contiguous())
+    assert np.array_equal(got, orc.round_f16(y_ref).reshape(y_ref.shape))
+    assert bool((Yw[:, rows:] == -7.0).all())
+    first = Yw.clone()
+    nm.nm_spmm_prefill(v, m, Xw, Y=Yw, cols=cols)
+    assert torch.equal(first.view(torch.int16), Yw.view(torch.int16))
+
+
+def test_prefill_argument_errors(nm):
+    L = nm.lib()
+    v = torch.zeros(64 * 32, dtype=torch.float16, device="cuda")
+    m = torch.zeros(64 * 2, dtype=torch.int32, device="cuda")
+    X = torch.zeros((16, 64), dtype=torch.float16, device="cuda")
+    Y = torch.zeros((16, 64), dtype=torch.float16, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()
+    assert L.nm_spmm_prefill(None, P(m), 64, 64, P(X), 64, 16, P(Y), 64, st) == 1
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 48, P(X), 64, 16, P(Y), 64, st) == 2   # cols % 32
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 32, 16, P(Y), 64, st) == 2   # ldx < cols
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 64, 16, P(Y), 32, st) == 2   # ldy < rows
+    assert L.nm_spmm_prefill(P(v) + 2, P(m), 64, 64, P(X), 64, 16, P(Y), 64, st) == 4
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X) + 2, 64, 16, P(Y), 64, st) == 4
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 64, 16, P(X), 64, st) == 7   # Y aliases X
+    assert L.nm_spmm_prefill_ex(P(v), P(m), 64, 64, P(X), 64, 16, P(Y), 64, 99, st) == 2
+    assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 64, 0, P(Y), 64, st) == 0    # T == 0
+    torch.cuda.synchronize()
+
+
+FULL = [(57344, 8192, 2048, (2, 4)), (10240, 8192, 1000, (16, 32)), (8192, 28672, 520, (8, 16))]
+
+
+@pytest.mark.parametrize("rows,cols,T,pat", FULL)
+def test_prefill_full_size_sampled(nm, orc, rows, cols, T, pat):
+    """Decoder-layer shapes at prefill lengths: sampled rows (tile edges
+    included) of sampled tokens (first and last included) against the oracle."""
+    N, M = pat
+    W = synth.weights(rows, cols, 0, synth.stream_id(71, rows, cols, 0))
+    X = synth.normal_f16((T, cols), 0, synth.stream_id(71, rows, cols, 1), synth.X_SIGMA)
+    Wd = to_dev(W)
+    v, m = nm.nm_pack(Wd, N, M)
+    del Wd
+    Y = nm.nm_spmm_prefill(v, m, to_dev(X))
+    torch.cuda.synchronize()
+    assert nm.nm_wait_timeouts() == 0
+    hv, hm = from_dev(v), from_dev(m)
+    row_ids = np.unique(np.concatenate([
+        synth.sample_rows(rows, 24, 0, synth.stream_id(72, rows)),
+        np.array([127, 128, rows - 129, rows - 128], dtype=np.int64)]))
+    toks = np.unique(np.concatenate([
+        synth.sample_rows(T, 6, 0, synth.stream_id(73, T)),
+        np.array([255, 256, 511, 512], dtype=np.int64)[np.array([255, 256, 511, 512]) < T]]))
+    Yh = from_dev(Y)
+    for t in toks:
+        y_ref, s = orc.spmv_rows_f64(hv, hm, cols, X[t], row_ids)
+        got = f16_to_f64(Yh[t, row_ids])
+        assert np.all(np.abs(got - y_ref) <= oracle.tolerance(s)), f"token {t}"

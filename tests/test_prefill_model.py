@@ -1,0 +1,209 @@
+"""CPU model of the tensor-core prefill kernel's shared-memory arithmetic.
+
+Mirrors csrc/prefill.cu's densify step bit for bit (popc rank, the two
+16-bit loads, the PTX prmt byte permutes that merge them and zero the absent
+columns, the 64-byte swizzle) and checks, before the kernel ever runs on a
+GPU, that:
+  * each stage's 128 x 32 tile is written exactly once per element, at the
+    byte the 64-byte TMA swizzle would put the same (row, column) -- so the
+    densified W tile and the X tile that TMA loads share one layout, the one
+    the MMA descriptor names;
+  * the densified row equals the unpacked row (kept values in place, +0
+    elsewhere) for every mask with 16 set bits;
+  * every shared-memory read stays inside the block's allocation, even for a
+    corrupt mask word;
+  * the shared-memory layout of each kernel variant fits a GB300 block and
+    keeps the swizzled tiles 1024-byte aligned.
+"""
+import numpy as np
+import pytest
+
+BM, BK, ROW_BYTES = 128, 32, 64
+A_BYTES, V_BYTES, M_BYTES = BM * ROW_BYTES, BM * 32, BM * 4
+DENSIFY_WARPS = 8
+ROWS_PER_WARP = BM // DENSIFY_WARPS
+VARIANTS = [(256, 2, 4), (256, 1, 6), (128, 1, 8), (64, 1, 8), (256, 2, 5)]
+SMEM_OPTIN = 232448  # bytes of dynamic shared memory a GB300 block may opt into
+
+
+def prmt(a, b, sel):
+    """PTX prmt.b32 default mode: byte i of the result is byte (sel_i & 7) of
+    the 8-byte value b:a, or that byte's sign replicated when sel_i & 8."""
+    src = [(a >> (8 * k)) & 0xFF for k in range(4)] + [(b >> (8 * k)) & 0xFF for k in range(4)]
+    out = 0
+    for i in range(4):
+        n = (sel >> (4 * i)) & 0xF
+        byte = src[n & 7]
+        if n & 8:
+            byte = 0xFF if byte & 0x80 else 0x00
+        out |= byte << (8 * i)
+    return out
+
+
+def popc(v):
+    return bin(v & 0xFFFFFFFF).count("1")
+
+
+MW, MT_SLOT = 4, BM * 4 * 4
+
+
+def mt_slots(stages):
+    return (stages + MW - 1 + MW - 1) // MW
+
+
+def layout(nmma, nb, stages, mt=True):
+    bn = nmma * nb
+    a_off = 0
+    b_off = a_off + stages * A_BYTES
+    v_off = b_off + stages * bn * ROW_BYTES
+    m_off = v_off + stages * V_BYTES
+    bar_off = m_off + (mt_slots(stages) * MT_SLOT if mt else stages * M_BYTES)
+    slot_off = bar_off + (3 * stages + 1) * 8
+    return dict(BN=bn, B_OFF=b_off, V_OFF=v_off, M_OFF=m_off, BAR_OFF=bar_off,
+                BYTES=slot_off + 16, SMEM=slot_off + 16 + 1024)
+
+
+def tma_sw64(r, byte_in_row):
+    """Byte offset TMA's 64-byte swizzle gives (row r, byte b) of a tile with
+    64-byte rows: 16-byte chunk bits [4:5] XOR address bits [7:8]."""
+    L = r * ROW_BYTES + byte_in_row
+    return L ^ (((L >> 7) & 3) << 4)
+
+
+def densify(masks_row_words, values_rows, sV=0, sM=None):
+    """Run the kernel's densify_stage on one stage; returns {phys byte: u32}
+    and the list of shared-memory byte addresses it read."""
+    writes, reads = {}, []
+    for dw in range(DENSIFY_WARPS):
+        for lane in range(32):
+            h, p = lane >> 4, lane & 15
+            b0 = 2 * p
+            below = (1 << b0) - 1
+            col_byte = (p & 3) * 4
+            chunk = p >> 2
+            for i in range(ROWS_PER_WARP // 2):
+                r = dw * ROWS_PER_WARP + 2 * i + h
+                m = int(masks_row_words[r])
+                reads.append(("M", 4 * r, r, 1))
+                c = popc(m & below)
+                q = (m >> b0) & 3
+                a0 = 32 * r + 2 * c
+                a1 = a0 + ((q & 1) << 1)
+                reads.append(("V", a0, r, q & 1))
+                reads.append(("V", a1, r, (q >> 1) & 1))
+                v0 = values_rows.get(a0, 0)
+                v1 = values_rows.get(a1, 0)
+                keep = prmt((q * 0x4080) & 0xFFFFFFFF, 0, 0x9988)
+                out = prmt(v0, v1, 0x5410) & keep
+                phys = r * ROW_BYTES + ((chunk ^ (i & 3)) << 4) + col_byte
+                assert phys not in writes, "element written twice"
+                writes[phys] = (out, r, 2 * p)
+    return writes, reads
+
+
+def random_masks(rng, rows, N, M):
+    """Valid N:M masks (16 set bits per 32-bit word) drawn group by group."""
+    words = np.zeros(rows, dtype=np.uint64)
+    for r in range(rows):
+        w = 0
+        for g in range(32 // M):
+            keep = rng.choice(M, size=N, replace=False)
+            for k in keep:
+                w |= 1 << (g * M + int(k))
+        words[r] = w
+    return words
+
+
+@pytest.mark.parametrize("N,M", [(2, 4), (4, 8), (8, 16), (16, 32)])
+def test_densify_equals_unpack_and_matches_tma_swizzle(N, M):
+    rng = np.random.default_rng(N)
+    masks = random_masks(rng, BM, N, M)
+    vals = rng.integers(1, 0x7BFF, size=(BM, 16), dtype=np.int64)   # nonzero fp16 bit patterns
+    values_rows = {}
+    for r in range(BM):
+        for k in range(16):
+            values_rows[32 * r + 2 * k] = int(vals[r, k])
+    writes, reads = densify(masks, values_rows)
+    assert len(writes) == BM * 16          # every (row, column pair) exactly once
+    for phys, (out, r, col) in writes.items():
+        assert phys == tma_sw64(r, 2 * col)
+        m = int(masks[r])
+        kept = [b for b in range(32) if (m >> b) & 1]
+        want = []
+        for b in (col, col + 1):
+            want.append(int(vals[r, kept.index(b)]) if b in kept else 0)
+        assert out == want[0] | (want[1] << 16), (r, col)
+    for kind, addr, r, used in reads:
+        if kind == "M":
+            assert addr == 4 * r
+        elif used:
+            assert 32 * r <= addr < 32 * r + 32        # a kept value comes from its own row
+        else:
+            # an absent column's load (result masked to +0) may sit one value
+            # past the row when every kept bit lies left of it: rank 16
+            assert 32 * r <= addr <= 32 * r + 32
+
+
+def test_corrupt_masks_read_inside_the_allocation():
+    """A word with more than 16 set bits makes the rank reach 31: the reads
+    run up to 64 bytes past the row, which for the last row of the last stage
+    lands in the mask ring that follows the value ring -- still inside the
+    block's shared memory for every variant."""
+    masks = np.full(BM, 0xFFFFFFFF, dtype=np.uint64)
+    _, reads = densify(masks, {})
+    vmax = max(a for k, a, _, _ in reads if k == "V")
+    assert vmax <= 32 * (BM - 1) + 2 * 31 + 2
+    for nmma, nb, stages in VARIANTS:
+        for mt in (True, False):
+            L = layout(nmma, nb, stages, mt)
+            last_stage_v = L["V_OFF"] + (stages - 1) * V_BYTES
+            assert last_stage_v + vmax + 2 <= L["BYTES"]
+
+
+def test_mask_slots_are_not_refilled_before_their_last_reader():
+    """With masks loaded by TMA (MW stages per box into mt_slots slots) the
+    producer refills a slot at stage kt + MW * slots only after the stage
+    STAGES earlier has been multiplied, i.e. after every densify of the
+    slot's previous MW stages."""
+    for _, _, stages in VARIANTS:
+        n = mt_slots(stages)
+        for kt in range(0, 64, MW):                # a group's first stage
+            refill = kt + MW * n                   # stage that reloads the same slot
+            done_before_refill = refill - stages   # MMA (so densify) finished for <= this
+            assert done_before_refill >= kt + MW - 1
+        assert MW * (n - 1) < stages + MW - 1      # and no slot more than needed
+
+
+@pytest.mark.parametrize("mt", [True, False])
+@pytest.mark.parametrize("nmma,nb,stages", VARIANTS)
+def test_layout_fits_and_is_aligned(nmma, nb, stages, mt):
+    L = layout(nmma, nb, stages, mt)
+    assert L["SMEM"] <= SMEM_OPTIN
+    assert 2 * L["SMEM"] > SMEM_OPTIN + 1024      # one block per SM: TMEM never contended
+    assert L["B_OFF"] % 1024 == 0 and (nmma * ROW_BYTES) % 1024 == 0
+    assert L["BAR_OFF"] % 8 == 0
+    tmem = 32
+    while tmem < L["BN"]:
+        tmem *= 2
+    assert tmem <= 512 and L["BN"] <= tmem
+    # epilogue: two warps per TMEM lane quadrant, 32 columns per tcgen05.ld
+    assert (L["BN"] // 2) % 32 == 0
+
+
+def test_instruction_and_smem_descriptors():
+    """Bit positions of the kind::f16 instruction descriptor and the 64-byte
+    swizzled K-major shared-memory descriptor the kernel builds."""
+    def idesc(M, N):
+        return (1 << 4) | ((N >> 3) << 17) | ((M >> 4) << 24)
+    d = idesc(128, 256)
+    assert (d >> 4) & 3 == 1                 # f32 accumulator
+    assert (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0   # f16 A and B
+    assert (d >> 15) & 1 == 0 and (d >> 16) & 1 == 0  # both K-major
+    assert (d >> 17) & 0x3F == 256 >> 3 and (d >> 24) & 0x1F == 128 >> 4
+    assert d & ((1 << 23) | (1 << 29) | 0xF) == 0      # reserved/sparsity bits clear
+
+    def sdesc(addr):
+        return ((addr >> 4) & 0x3FFF) | (1 << 16) | ((512 >> 4) << 32) | (1 << 46) | (4 << 61)
+    s = sdesc(0x2C400 + 32)
+    assert s & 0x3FFF == (0x2C400 + 32) >> 4
+    assert (s >> 32) & 0x3FFF == 32 and (s >> 46) & 3 == 1 and s >> 61 == 4
