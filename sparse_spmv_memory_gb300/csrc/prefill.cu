@@ -12,11 +12,13 @@
 //  * A block owns a tile of BM = 128 rows of W and BN = NB * NMMA tokens; its
 //    fp32 accumulator D (128 x BN) lives in tensor memory, row m in TMEM lane
 //    m.  K advances one mask word (32 columns) per pipeline stage.
-//  * Warp 0 (producer): per stage, a TMA load of the token tile of X
-//    (BN x 32 fp16, 64-byte swizzle) and of the tile's compact values
-//    (128 rows x 16 fp16), plus a 4-byte cp.async of each row's mask word;
-//    all complete on the stage's "full" mbarrier.
-//  * Warps 2..9 (densify): expand each row's 16 kept values into the 32
+//  * Two producer warps, each a short chain of asynchronous copies per stage
+//    so that the two run side by side: warp 0 loads the token tile of X by
+//    TMA (BN x 32 fp16, 64-byte swizzle); warp 2 loads the tile's compact
+//    values (128 rows x 16 fp16) by TMA and its mask words (by TMA, four
+//    stages per box, when the mask pitch allows it, else by cp.async).  Both
+//    complete on the stage's "full" mbarrier.
+//  * Warps 3..18 (densify): expand each row's 16 kept values into the 32
 //    columns of a K-major, 64-byte-swizzled fp16 tile in shared memory, the
 //    layout the MMA descriptor names.  A lane builds two adjacent columns:
 //    the rank of its first column among the word's set bits (one popc) is the
@@ -24,7 +26,7 @@
 //  * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (M = 128,
 //    N = NMMA, K = 16; two per stage and N-part) on the densified tile and the
 //    X tile, and tcgen05.commit frees the stage when those MMAs are done.
-//  * Epilogue (warps 2..9): tcgen05.ld of the accumulator, fp32 -> fp16 RNE,
+//  * Epilogue (warps 3..18): tcgen05.ld of the accumulator, fp32 -> fp16 RNE,
 //    stores to Y[t][r].
 //  * Every mbarrier wait gives up after kWaitLimitNs (counted in
 //    g_wait_timeouts); the roles then skip to teardown, which waits for the
@@ -50,9 +52,11 @@ constexpr int V_BYTES = BM * 32;       // compact values: 16 fp16 per row
 constexpr int M_BYTES = BM * 4;        // one mask word per row (cp.async ring)
 constexpr int MW = 4;                  // mask words per TMA box (16 bytes per row)
 constexpr int MT_SLOT = BM * MW * 4;   // 2 KiB: the masks of MW consecutive stages
-constexpr int DENSIFY_WARPS = 8;
-constexpr int THREADS = (2 + DENSIFY_WARPS) * 32;
-constexpr int ROWS_PER_WARP = BM / DENSIFY_WARPS;  // 16: two rows per pass
+constexpr int DENSIFY_WARPS = 16;
+constexpr int FIRST_DENSIFY_WARP = 3;
+constexpr int THREADS = (FIRST_DENSIFY_WARP + DENSIFY_WARPS) * 32;
+constexpr int ROWS_PER_WARP = BM / DENSIFY_WARPS;  // 8: two rows per pass
+static_assert(ROWS_PER_WARP % 8 == 0 || ROWS_PER_WARP == 8, "swizzle phase below needs row groups of 8");
 
 constexpr uint32_t tmem_cols_for(int n) {
   return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
@@ -80,10 +84,9 @@ struct Layout {
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
-  static constexpr uint32_t TX_BYTES = V_BYTES + B_BYTES;  // + MT_SLOT when masks load
   static_assert(!MT || MW * MT_SLOTS >= STAGES + MW - 1, "mask slot reused too early");
   static_assert(NMMA % 16 == 0 && NMMA >= 16 && NMMA <= 256, "tcgen05 M=128 needs N in 16..256");
-  static_assert(BN >= 64 && BN <= 512, "epilogue splits BN over two warps of 32 columns");
+  static_assert(BN >= 64 && BN <= 512 && BN % 32 == 0, "epilogue reads 32-column chunks");
   static_assert(B_OFF % 1024 == 0 && (NMMA * ROW_BYTES) % 1024 == 0, "swizzled tiles 1024-aligned");
 };
 
@@ -122,13 +125,13 @@ __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t
     const uint32_t keep = prmt(q[i] * 0x4080u, 0u, 0x9988u);
     const uint32_t out = prmt(v0[i], v1[i], 0x5410u) & keep;
     // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3, and
-    // (r >> 1) & 3 == i & 3 because dw * 16 is a multiple of 8.
+    // (r >> 1) & 3 == i & 3 because dw * ROWS_PER_WARP is a multiple of 8.
     const uint32_t phys = r * ROW_BYTES + ((chunk ^ (uint32_t)(i & 3)) << 4) + col_byte;
     sts_u32(sA + phys, out);
   }
 }
 
-template <int NMMA, int NB, int STAGES, bool MT>
+template <int NMMA, int NB, int STAGES, int G, bool MT>
 __global__ void __launch_bounds__(THREADS, 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), MT ? 1 : 1 + 32);    // expect_tx arrival (+ 32 cp.async arrivals)
+      mbar_init(full(s), MT ? 2 : 2 + 32);    // two expect_tx arrivals (+ 32 cp.async arrivals)
       mbar_init(empty(s), 1);                 // tcgen05.commit
       mbar_init(afull(s), DENSIFY_WARPS);     // one arrival per densify warp
     }
@@ -171,70 +174,100 @@ __global__ void __launch_bounds__(THREADS, 1)
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(slot) : "memory");
 
   if (warp == 0) {
-    // ---- producer ------------------------------------------------------
-    int issued = 0;
-    for (int kt = 0; kt < words; ++kt) {
-      const int s = kt % STAGES, u = kt / STAGES;
-      int ok = 1;
-      if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1);
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
-      if (lane == 0) {
-        const bool mask_load = MT && kt % MW == 0;
-        mbar_arrive_expect_tx(full(s), L::TX_BYTES + (mask_load ? MT_SLOT : 0));
-        if (mask_load)
-          tma_load_2d(sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT, &tm_m, kt, (int)r0, full(s));
-        tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
+    // ---- X producer: the token tile of each stage -----------------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int kt = 0; kt < words; ++kt) {
+        const int s = kt % STAGES, u = kt / STAGES;
+        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1)) break;
+        mbar_arrive_expect_tx(full(s), L::B_BYTES);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
           tma_load_2d(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES, &tm_x, kt * BK,
                       (int)(n0 + j * NMMA), full(s));
+        issued = kt + 1;
       }
-      if (!MT) {
-#pragma unroll
-        for (int i = 0; i < BM / 32; ++i) {
-          const int rr = lane + 32 * i;
-          const int64_t gr = r0 + rr;
-          const bool in = gr < rows;
-          cp_async_4(sM + s * M_BYTES + 4u * rr, masks + (in ? gr : 0) * words + kt, in ? 4u : 0u);
-        }
-        cp_async_arrive_noinc(full(s));
-      }
-      issued = kt + 1;
-    }
-    cp_async_wait_all();
-    // Teardown must not free shared memory under copies still in flight: wait
-    // (bounded) for the last stages this warp issued.
-    if (lane == 0) {
+      // Teardown must not free shared memory under copies still in flight:
+      // wait (bounded) for the last stages issued.
       const int first = issued > STAGES ? issued - STAGES : 0;
       for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---- W producer: compact values (and mask words) of each stage ----------
+    // With MT one lane issues TMA; without, all lanes gather the mask words
+    // by cp.async, each arriving on the stage barrier when its copies land.
+    if (!MT || lane == 0) {
+      int issued = 0;
       for (int kt = 0; kt < words; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
-        if (!mbar_wait(full(s), u & 1)) break;
-        if (!mbar_wait(afull(s), u & 1)) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint64_t ad = smem_desc_sw64(sA + s * A_BYTES + ks * 32);
-#pragma unroll
-          for (int j = 0; j < NB; ++j) {
-            const uint64_t bd = smem_desc_sw64(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES + ks * 32);
-            mma_f16(tmem_base + (uint32_t)(j * NMMA), ad, bd, idesc, (kt | ks) != 0);
-          }
+        int ok = 1;
+        if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1);
+        if (!MT) ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          const bool mask_load = MT && kt % MW == 0;
+          mbar_arrive_expect_tx(full(s), V_BYTES + (mask_load ? MT_SLOT : 0));
+          if (mask_load)
+            tma_load_2d(sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT, &tm_m, kt, (int)r0, full(s));
+          tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
         }
-        mma_commit(empty(s));
+        if (!MT) {
+#pragma unroll
+          for (int i = 0; i < BM / 32; ++i) {
+            const int rr = lane + 32 * i;
+            const int64_t gr = r0 + rr;
+            const bool in = gr < rows;
+            cp_async_4(sM + s * M_BYTES + 4u * rr, masks + (in ? gr : 0) * words + kt,
+                       in ? 4u : 0u);
+          }
+          cp_async_arrive_noinc(full(s));
+        }
+        issued = kt + 1;
+      }
+      if (!MT) cp_async_wait_all();
+      if (lane == 0) {
+        const int first = issued > STAGES ? issued - STAGES : 0;
+        for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer ----------------------------------------------------
+    // Waits only on the densify barriers, and on one per G stages: each
+    // densify warp saw the stage's "full" barrier complete (so the TMA-loaded
+    // X tile is visible through its release-arrive) and arrives on the stages
+    // in order, so afull(kt + G - 1) complete implies the earlier ones are.
+    // A barrier test costs the single issuing thread a few hundred cycles,
+    // a whole stage's budget when N is small (G = 2 there); with large N the
+    // wait for a second stage would delay the first stage's MMAs (G = 1).
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
+      for (int kt = 0; kt < words; kt += G) {
+        const int last = kt + G - 1 < words ? kt + G - 1 : words - 1;
+        if (!mbar_wait(afull(last % STAGES), (last / STAGES) & 1)) break;
+        tc_fence_after_sync();
+        for (int k = kt; k <= last; ++k) {
+          const int s = k % STAGES;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint64_t ad = smem_desc_sw64(sA + s * A_BYTES + ks * 32);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const uint64_t bd =
+                  smem_desc_sw64(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES + ks * 32);
+              mma_f16(tmem_base + (uint32_t)(j * NMMA), ad, bd, idesc, (k | ks) != 0);
+            }
+          }
+          mma_commit(empty(s));
+        }
       }
       mma_commit(accum);  // also after an early exit: completes once issued MMAs finish
     }
     __syncwarp();
   } else {
     // ---- densify, then epilogue -----------------------------------------
-    const int dw = warp - 2;
+    const int dw = warp - FIRST_DENSIFY_WARP;
     bool ok = true;
     for (int kt = 0; kt < words; ++kt) {
       const int s = kt % STAGES, u = kt / STAGES;
@@ -257,12 +290,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // tcgen05.ld is a warp-wide instruction: the whole warp reads or none does.
     if (__all_sync(0xFFFFFFFFu, ok)) {
       const int quad = warp & 3;              // TMEM lanes 32*quad .. +31
-      const int half = dw >> 2;               // which half of the BN columns
+      const int qi = dw >> 2;                 // this warp's index among its quadrant's warps
+      constexpr int QW = DENSIFY_WARPS / 4;   // warps per quadrant, striding the columns
       const int64_t r = r0 + 32 * quad + lane;
       const bool row_ok = r < rows;
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * quad) << 16);
 #pragma unroll 1
-      for (int c0 = half * (L::BN / 2); c0 < (half + 1) * (L::BN / 2); c0 += 32) {
+      for (int c0 = qi * 32; c0 < L::BN; c0 += QW * 32) {
         uint32_t v[32];
         tmem_ld_32(tbase + (uint32_t)c0, v);
         tmem_ld_wait();
@@ -287,9 +321,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---- host ------------------------------------------------------------------
 struct Variant {
-  int nmma, nb, stages;
+  int nmma, nb, stages, g;
 };
-constexpr Variant kVariants[] = {{256, 2, 4}, {256, 1, 6}, {128, 1, 8}, {64, 1, 8}, {256, 2, 5}};
+constexpr Variant kVariants[] = {
+    {256, 2, 4, 1}, {256, 1, 6, 1}, {128, 1, 8, 2}, {64, 1, 8, 2}, {256, 2, 5, 1}};
 constexpr int kVariantCount = sizeof(kVariants) / sizeof(kVariants[0]);
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -325,7 +360,7 @@ static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMMA, int NB, int STAGES, bool MT>
+template <int NMMA, int NB, int STAGES, int G, bool MT>
 static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
   using L = Layout<NMMA, NB, STAGES, MT>;
   CUtensorMap tm_v, tm_x, tm_m;
@@ -339,7 +374,7 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
       !encode_2d(&tm_x, p.X, (uint64_t)p.words * 32, (uint64_t)p.T, (uint64_t)p.ldx * 2, BK,
                  NMMA, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, MT>;
+  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, G, MT>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -360,11 +395,11 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
 
 // Mask words by TMA when the mask array allows it (16-byte aligned, row pitch
 // words * 4 a multiple of 16: every decoder shape), else by cp.async.
-template <int NMMA, int NB, int STAGES>
+template <int NMMA, int NB, int STAGES, int G>
 static cudaError_t launch_tc(const SpmmTcParams& p, cudaStream_t stream) {
   const bool mt = p.words % 4 == 0 && (reinterpret_cast<uintptr_t>(p.masks) & 15) == 0;
-  return mt ? launch_tc_mt<NMMA, NB, STAGES, true>(p, stream)
-            : launch_tc_mt<NMMA, NB, STAGES, false>(p, stream);
+  return mt ? launch_tc_mt<NMMA, NB, STAGES, G, true>(p, stream)
+            : launch_tc_mt<NMMA, NB, STAGES, G, false>(p, stream);
 }
 
 }  // namespace tc
@@ -387,11 +422,11 @@ int spmm_tc_block_tokens(int variant) {
 
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
   switch (variant) {
-    case 0: return tc::launch_tc<256, 2, 4>(p, stream);
-    case 1: return tc::launch_tc<256, 1, 6>(p, stream);
-    case 2: return tc::launch_tc<128, 1, 8>(p, stream);
-    case 3: return tc::launch_tc<64, 1, 8>(p, stream);
-    case 4: return tc::launch_tc<256, 2, 5>(p, stream);
+    case 0: return tc::launch_tc<256, 2, 4, 1>(p, stream);
+    case 1: return tc::launch_tc<256, 1, 6, 1>(p, stream);
+    case 2: return tc::launch_tc<128, 1, 8, 2>(p, stream);
+    case 3: return tc::launch_tc<64, 1, 8, 2>(p, stream);
+    case 4: return tc::launch_tc<256, 2, 5, 1>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
