@@ -20,6 +20,10 @@ Timing: CUDA graph replays timed with CUDA events on the launching stream,
 W untimed warm-up steps, then exactly K timed steps between barriers and
 device synchronisation; L2 is defeated by the rotating set (stated in config).
 
+``--prefill T`` times the prefill regime instead: the same layer's four
+projections for T tokens at once through nm_spmm_prefill (tensor cores),
+against cuBLAS fp16 GEMM on the dense weights (dense-equivalent TFLOP/s).
+
 ``--impl reference`` times the CPU oracle instead (the slow reference arm).
 Multi-GPU (torchrun, N ranks): every rank runs an independent replica (the
 path has no exchange step); value = all ranks' bytes / the slowest rank's time.
@@ -42,7 +46,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "N:M SpMV µs/call & achieved HBM GB/s (% peak) at batch 1; speedup vs dense GEMV"
+PREFILL_METRIC = ("N:M prefill SpMM dense-equivalent TFLOP/s (2*rows*cols*tokens per call) on the "
+                  "tensor cores; speedup vs cuBLAS fp16 GEMM")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 NOMINAL_HBM_GBS = 7900.0
 
 WORKLOADS = {
@@ -200,24 +207,44 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def tensor_peak(seconds_timed: float):
+    """Measured dense bf16 tensor peak (fp16 runs at the same nominal rate):
+    the sustained figure for a timed region of a second or more, else burst."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if seconds_timed >= 1.0 and "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured sustained (bf16_tflops_sustained)"
+        return float(d["bf16_tflops"]), "measured burst (bf16_tflops)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback 1900 TFLOP/s"
+
+
+def kernel_source_hash(names=("spmv.cu", "device.cuh", "split.cuh")) -> str:
+    """Hash of the files that define a kernel's code (by default the SpMV
+    kernels'); a committed ncu traffic record is used only while it matches."""
     h = hashlib.sha256()
-    for name in ("spmv.cu", "device.cuh", "split.cuh", "kernels.h"):
+    for name in names:
         with open(os.path.join(ROOT, "sparse_spmv_memory_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(shape_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+PREFILL_SOURCES = ("prefill.cu", "tc.cuh", "device.cuh")
+
+
+def ncu_traffic(shape_key: str, record="nm_spmv_traffic.json", sources=None):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the kernel source as it is now (else None)."""
-    p = os.path.join(ROOT, "profiles", "nm_spmv_traffic.json")
+    p = os.path.join(ROOT, "profiles", record)
     try:
         with open(p) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    want = kernel_source_hash(sources) if sources else kernel_source_hash()
+    if d.get("kernel_source_hash") != want:
         return None
     e = d.get("per_launch", {}).get(shape_key)
     return None if e is None else float(e["dram_bytes"])
@@ -629,6 +656,165 @@ def run_gpu(args):
     return out
 
 
+def prefill_flops(mats, T):
+    """Dense-equivalent flops of one pass of the matrices over T tokens."""
+    return sum(2.0 * r * c * T for _, r, c in mats)
+
+
+def oracle_prefill_rate(mats, pattern, seconds: float):
+    """The oracle on a bounded sample: the sampled rows of every matrix for a
+    handful of tokens; returns (dense-equivalent TFLOP/s, description, s)."""
+    rows_per, _, _, _ = oracle_sample(mats, pattern, seconds / 4)
+    orc, packed = oracle_pack_sample(mats, pattern, rows_per)
+    import synth
+    tokens = 4
+    xs = [[synth.activations(cols, 0, synth.stream_id(3, mi, t)) for t in range(tokens)]
+          for mi, (_, _, cols, _, _) in enumerate(packed)]
+    t0 = time.perf_counter()
+    fl = 0.0
+    for mi, (v, m, cols, _, n) in enumerate(packed):
+        for t in range(tokens):
+            orc.spmv_f64(v, m, cols, xs[mi][t])
+            fl += 2.0 * n * cols
+    dt = time.perf_counter() - t0
+    desc = (f"first {rows_per} rows of each of the {len(mats)} matrices x {tokens} tokens, "
+            f"{pattern[0]}:{pattern[1]}, oracle unpack + double matvec per token, 1 thread")
+    return fl / dt / 1e12, desc, dt
+
+
+def run_prefill(args):
+    """Prefill regime: Y = W X for T tokens per call, every matrix of the
+    workload, ``args.prefill_layers`` logical layers per step cycling two
+    packed slots (the call is compute-bound, so L2 residency is immaterial)."""
+    import torch
+    import synth
+    import sparse_spmv_memory_gb300 as nm
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    nm.lib()
+    nm.nm_wait_timeouts(reset=True)
+    mats = WORKLOADS[args.workload]
+    T, layers = args.prefill, args.prefill_layers
+    stream = torch.cuda.Stream(device)
+    head = tuple(int(t) for t in args.pattern.split(":"))
+    dense, _ = make_dense(mats, device, 1)
+    X = []
+    for mi, (_, rows, cols) in enumerate(mats):
+        h = torch.empty((T, cols), dtype=torch.int16, pin_memory=True)
+        synth.normal_f16_into(h.data_ptr(), T * cols, 0, synth.stream_id(4, mi, T), synth.X_SIGMA)
+        X.append(h.to(device).view(torch.float16))
+    Y = [torch.empty((T, r), dtype=torch.float16, device=device) for _, r, _ in mats]
+    slots = pack_slots(nm, dense, head, 2)
+
+    def run_sparse():
+        for l in range(layers):
+            for i, (v, m) in enumerate(slots[l % 2]):
+                nm.nm_spmm_prefill(v, m, X[i], Y=Y[i])
+
+    with ClockSampler(local) as cs:
+        per, total = time_graph(run_sparse, args.steps, args.warmup, stream, clock=cs)
+    clocks = cs.summary()
+    k = len(per)
+    per_matrix = {}
+    for i, (name, rows, cols) in enumerate(mats):
+        def one(i=i):
+            for l in range(layers):
+                v, m = slots[l % 2][i]
+                nm.nm_spmm_prefill(v, m, X[i], Y=Y[i])
+        p1, t1 = time_graph(one, 5, 3, stream)
+        us = statistics.median(p1) * 1e3 / layers
+        per_matrix[name] = {"shape": f"{rows}x{cols}", "tokens": T, "us_per_call": round(us, 1),
+                            "TFLOP_s": round(2.0 * rows * cols * T / us / 1e6, 1)}
+
+    # end to end: pinned host X in and Y out every step, eager public calls
+    x_host = [x.cpu().pin_memory() for x in X]
+    y_host = [torch.empty(y.shape, dtype=torch.float16, pin_memory=True) for y in Y]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for i in range(len(mats)):
+                X[i].copy_(x_host[i], non_blocking=True)
+            run_sparse()
+            for i in range(len(mats)):
+                y_host[i].copy_(Y[i], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            for i in range(len(mats)):
+                X[i].copy_(x_host[i], non_blocking=True)
+            run_sparse()
+            for i in range(len(mats)):
+                y_host[i].copy_(Y[i], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    timeouts = nm.nm_wait_timeouts()
+    del slots
+    torch.cuda.empty_cache()
+
+    # cuBLAS on the dense weights, same tokens and layer count
+    Yd = [torch.empty_like(y) for y in Y]
+
+    def run_dense():
+        for l in range(layers):
+            for i, W in enumerate(dense):
+                torch.mm(X[i], W.t(), out=Yd[i])
+
+    dper, dtotal = time_graph(run_dense, max(3, args.steps // 2), args.warmup, stream)
+
+    step_flops = layers * prefill_flops(mats, T)
+    units, secs = aggregate(step_flops * k, total)
+    tf = units / secs / 1e12
+    peak, peak_kind = tensor_peak(total)
+    d_tf = step_flops * len(dper) / dtotal / 1e12
+    dom = max(mats, key=lambda m: m[1] * m[2])
+    out = {
+        "metric": PREFILL_METRIC, "value": round(tf, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": k, "warmup": args.warmup, "ms_per_step": round(secs / k * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 in/out, fp32 accumulate (tensor cores, kind::f16)",
+        "data": "synthetic (seeded N(0,0.02) fp16 weights, top-N |w| per M-group; N(0,1) fp16 X)",
+        "config": {
+            "workload": (f"{args.workload} x{layers} layers, prefill {T} tokens, "
+                         + ", ".join(f"{n} {r}x{c}" for n, r, c in mats)),
+            "pattern": f"{head[0]}:{head[1]}", "calls_per_step": layers * len(mats),
+            "physical_slots": 2,
+            "l2_defeat": "not needed: compute-bound (each call re-reads its tiles from L2 by design)",
+            "parallelism": f"replicas x{world}", "kernel_variant": "library default for T",
+        },
+        "gpu_launches": layers * len(mats) * k,
+        "us_per_call": per_matrix,
+        "cublas": {"TFLOP_s": round(d_tf, 1), "ms_per_step": round(dtotal / len(dper) * 1e3, 3),
+                   "kernel": "torch.mm (cuBLAS) fp16 on the dense weights"},
+        "speedup_vs_dense": round(tf / d_tf, 4),
+        "roofline": {"bound": "tensor", "kernel": "nm_spmm_prefill (spmm_tc_kernel)",
+                     "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(f"{dom[1]}x{dom[2]}x{T}", "nm_spmm_prefill_traffic.json",
+                                            PREFILL_SOURCES),
+                     "traffic_shape": f"{dom[1]}x{dom[2]}, {T} tokens",
+                     "achieved_basis": ("dense-equivalent MMA flops of the timed region's launches "
+                                        "/ the region's CUDA-event device time (a lower bound); "
+                                        "fp16 and bf16 share the nominal dense rate"),
+                     "dominant_shape": f"{dom[1]}x{dom[2]}"},
+        "e2e": {"value": round(step_flops * args.steps / e2e_s / 1e12, 1), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(x.numel() * 2 for x in X),
+                "d2h_bytes_per_step": sum(y.numel() * 2 for y in Y),
+                "ms_per_step": round(e2e_s / args.steps * 1e3, 3),
+                "path": "Python binding -> C ABI nm_spmm_prefill per call, eager, pinned host X/Y"},
+        "clocks": clocks, "wait_timeouts": timeouts,
+    }
+    if rank == 0 and world == 1 and args.cpu:
+        rate, desc, dt = oracle_prefill_rate(mats, head, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": 1,
+                               "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    return out
+
+
 def run_reference(args):
     """The reference arm: the plain CPU oracle, timed as it stands."""
     world, rank, _ = dist_env()
@@ -636,6 +822,21 @@ def run_reference(args):
         return None
     mats = WORKLOADS[args.workload]
     head = tuple(int(t) for t in args.pattern.split(":"))
+    if args.prefill:
+        secs = max(1.0, args.ref_seconds / 4)
+        rate, desc, dt = oracle_prefill_rate(mats, head, secs)
+        return {
+            "impl": "reference", "metric": PREFILL_METRIC, "value": round(rate, 6),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": 1, "warmup": 0,
+            "ms_per_step": round(dt * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": f"{args.workload}, prefill {args.prefill} tokens, oracle sample",
+                       "pattern": args.pattern},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(rate, 6),
+                             "unit": "TFLOP/s"},
+            "e2e": {"value": round(rate, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
     per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
     rows_per, _, _, desc = oracle_sample(mats, head, per_step)
     orc, packed = oracle_pack_sample(mats, head, rows_per)
@@ -674,6 +875,11 @@ def parse(argv=None):
     ap.add_argument("--batch", type=int, default=1,
                     help="tokens per step: 1 = nm_spmv (the headline); 2..8 = nm_spmm, with "
                          "cuBLAS (torch.mm) as the dense reference")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="tokens per call for the prefill regime (nm_spmm_prefill on the tensor "
+                         "cores, cuBLAS fp16 GEMM as the dense reference); 0 = decode (default)")
+    ap.add_argument("--prefill-layers", type=int, default=4,
+                    help="logical layers per prefill step")
     ap.add_argument("--layers", type=int, default=None,
                     help="logical layers per step (default: the model's layer count)")
     ap.add_argument("--slots", type=int, default=16, help="physical sparse layer slots")
@@ -691,6 +897,8 @@ def parse(argv=None):
     a = ap.parse_args(argv)
     if not 1 <= a.batch <= 8:
         ap.error("--batch must be in 1..8")
+    if a.prefill < 0 or (a.prefill and a.batch != 1):
+        ap.error("--prefill takes a positive token count and no --batch")
     if a.layers is None:
         a.layers = LAYERS[a.workload]
     if a.warmup < 3:
@@ -708,7 +916,10 @@ def main(argv=None):
             import torch
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
-    out = run_gpu(args) if args.impl == "ours" else run_reference(args)
+    if args.impl == "reference":
+        out = run_reference(args)
+    else:
+        out = run_prefill(args) if args.prefill else run_gpu(args)
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     if world > 1:

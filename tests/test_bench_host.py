@@ -90,3 +90,24 @@ def test_reference_arm_other_ranks_exit_quietly():
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.parse(["--warmup", "2"])
+
+
+def test_prefill_reference_arm_and_flop_accounting():
+    mats = bench.WORKLOADS["llama33_70b_layer"]
+    assert bench.prefill_flops(mats, 2) == 2 * 2 * sum(r * c for _, r, c in mats)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--prefill", "512", "--ref-seconds", "4", "--workload", "single_4096"],
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    d = json.loads(lines[-1])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["metric"] == bench.PREFILL_METRIC
+
+
+def test_prefill_argument_checks():
+    assert bench.parse(["--prefill", "2048"]).prefill == 2048
+    with pytest.raises(SystemExit):
+        bench.parse(["--prefill", "64", "--batch", "4"])
+    with pytest.raises(SystemExit):
+        bench.parse(["--prefill", "-1"])
