@@ -489,7 +489,11 @@ int nm_spmm_prefill_ex(const void* values, const uint32_t* masks, int64_t rows, 
   p.rows = rows;
   p.words = (int)(cols / 32);
   p.T = T;
-  if (variant < 0) variant = spmm_tc_default_variant(T);
+  if (variant < 0) {
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+    variant = spmm_tc_default_variant(rows, T, d.sms);
+  }
   cudaError_t e = launch_spmm_tc(p, variant, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }

@@ -107,7 +107,7 @@ struct SpmmTcParams {
 };
 
 int spmm_tc_variant_count();
-int spmm_tc_default_variant(int64_t T);
+int spmm_tc_default_variant(int64_t rows, int64_t T, int sms);
 int spmm_tc_block_tokens(int variant);
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream);
 // Number of bounded mbarrier waits that gave up since the last reset.

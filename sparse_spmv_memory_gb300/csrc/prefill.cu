@@ -52,11 +52,11 @@ constexpr int V_BYTES = BM * 32;       // compact values: 16 fp16 per row
 constexpr int M_BYTES = BM * 4;        // one mask word per row (cp.async ring)
 constexpr int MW = 4;                  // mask words per TMA box (16 bytes per row)
 constexpr int MT_SLOT = BM * MW * 4;   // 2 KiB: the masks of MW consecutive stages
-constexpr int DENSIFY_WARPS = 16;
+// Densify warps per block (DW, a kernel parameter) follow the producer and
+// MMA warps.  16 measured best on GB300: 8 left the per-stage chains
+// exposed, 24 lost to the extra shared-memory and issue contention.
 constexpr int FIRST_DENSIFY_WARP = 3;
-constexpr int THREADS = (FIRST_DENSIFY_WARP + DENSIFY_WARPS) * 32;
-constexpr int ROWS_PER_WARP = BM / DENSIFY_WARPS;  // 8: two rows per pass
-static_assert(ROWS_PER_WARP % 8 == 0 || ROWS_PER_WARP == 8, "swizzle phase below needs row groups of 8");
+__host__ __device__ constexpr int threads_for(int dw) { return (FIRST_DENSIFY_WARP + dw) * 32; }
 
 constexpr uint32_t tmem_cols_for(int n) {
   return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
@@ -79,8 +79,9 @@ struct Layout {
   static constexpr int M_OFF = V_OFF + STAGES * V_BYTES;
   static constexpr int MT_SLOTS = (STAGES + MW - 1 + MW - 1) / MW;
   static constexpr int M_REGION = MT ? MT_SLOTS * MT_SLOT : STAGES * M_BYTES;
-  static constexpr int BAR_OFF = M_OFF + M_REGION;  // full, empty, afull, accum
-  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1) * 8;
+  // barriers: full, empty, afull (per stage), accum, mfull (per mask slot)
+  static constexpr int BAR_OFF = M_OFF + M_REGION;
+  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1 + MT_SLOTS) * 8;
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
@@ -90,21 +91,23 @@ struct Layout {
   static_assert(B_OFF % 1024 == 0 && (NMMA * ROW_BYTES) % 1024 == 0, "swizzled tiles 1024-aligned");
 };
 
-// 128 rows x 32 columns: lane (h, p) builds columns 2p, 2p+1 of rows
-// r_i = dw * 16 + 2 i + h, i = 0..7.  The shared-memory accesses are issued
-// in three batches (8 mask words, 16 values, 8 stores) so that each batch's
-// latency is paid once per stage rather than once per row.
+// RPW rows x 32 columns of one stage: lane (h, p) of warp wg builds columns
+// 2p, 2p+1 of rows r_i = wg * RPW + 2 i + h, i < RPW / 2.  The shared-memory
+// accesses are issued in three batches (mask words, values, stores) so that
+// each batch's latency is paid once per stage rather than once per row.
 // sMw: this stage's mask word of row 0; mstride: bytes from one row's word
 // to the next row's.
+template <int RPW>
 __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t sMw,
-                                              uint32_t mstride, int dw, int lane) {
-  constexpr int R = ROWS_PER_WARP / 2;
+                                              uint32_t mstride, int wg, int lane) {
+  static_assert(RPW % 8 == 0, "the swizzle phase below needs whole groups of 8 rows");
+  constexpr int R = RPW / 2;
   const int h = lane >> 4, p = lane & 15;
   const uint32_t b0 = 2u * p;
   const uint32_t below = (1u << b0) - 1u;       // columns of the word left of 2p
   const uint32_t col_byte = (uint32_t)(p & 3) * 4u;
   const uint32_t chunk = (uint32_t)(p >> 2);
-  const uint32_t r_first = (uint32_t)(dw * ROWS_PER_WARP + h);
+  const uint32_t r_first = (uint32_t)(wg * RPW + h);
   uint32_t m[R], q[R], v0[R], v1[R];
 #pragma unroll
   for (int i = 0; i < R; ++i) m[i] = lds_u32(sMw + mstride * (r_first + 2 * i));
@@ -125,18 +128,28 @@ __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t
     const uint32_t keep = prmt(q[i] * 0x4080u, 0u, 0x9988u);
     const uint32_t out = prmt(v0[i], v1[i], 0x5410u) & keep;
     // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3, and
-    // (r >> 1) & 3 == i & 3 because dw * ROWS_PER_WARP is a multiple of 8.
+    // (r >> 1) & 3 == i & 3 because wg * RPW is a multiple of 8.
     const uint32_t phys = r * ROW_BYTES + ((chunk ^ (uint32_t)(i & 3)) << 4) + col_byte;
     sts_u32(sA + phys, out);
   }
 }
 
-template <int NMMA, int NB, int STAGES, int G, bool MT>
-__global__ void __launch_bounds__(THREADS, 1)
+// DG: the densify warps form DG groups; group g expands stages g, g + DG,
+// ... with 128 / (16 / DG) rows per warp.  Each stage costs a warp a fixed
+// chain of barrier waits, fences and arrivals (hundreds of cycles of
+// latency) besides its rows, so with DG groups that chain overlaps DG stages.
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW, bool MT>
+__global__ void __launch_bounds__(threads_for(DW), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
                    __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy) {
   using L = Layout<NMMA, NB, STAGES, MT>;
+  static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
+  static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
+  static_assert(threads_for(DW) <= 1024, "a block has at most 1024 threads");
+  static_assert(DG <= MW, "every densify group must read every mask box, in order");
+  constexpr int WPG = DW / DG;             // warps per densify group
+  constexpr int RPW = BM / WPG;            // rows per warp and stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -146,6 +159,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto empty = [&](int s) { return bars + 8u * (STAGES + s); };
   auto afull = [&](int s) { return bars + 8u * (2 * STAGES + s); };
   const uint32_t accum = bars + 8u * (3 * STAGES);
+  // A mask box serves MW consecutive stages that may belong to different
+  // densify groups, so it completes on a barrier of its own.
+  auto mfull = [&](int slot) { return bars + 8u * (3 * STAGES + 1 + slot); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = (int64_t)blockIdx.y * BM;
@@ -155,9 +171,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), MT ? 2 : 2 + 32);    // two expect_tx arrivals (+ 32 cp.async arrivals)
       mbar_init(empty(s), 1);                 // tcgen05.commit
-      mbar_init(afull(s), DENSIFY_WARPS);     // one arrival per densify warp
+      mbar_init(afull(s), WPG);               // one arrival per warp of the stage's group
     }
     mbar_init(accum, 1);
+    for (int m = 0; m < L::MT_SLOTS; ++m) mbar_init(mfull(m), 1);
     fence_mbar_init();
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_x);
@@ -206,10 +223,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!MT) ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          const bool mask_load = MT && kt % MW == 0;
-          mbar_arrive_expect_tx(full(s), V_BYTES + (mask_load ? MT_SLOT : 0));
-          if (mask_load)
-            tma_load_2d(sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT, &tm_m, kt, (int)r0, full(s));
+          if (MT && kt % MW == 0) {
+            const int ms = (kt / MW) % L::MT_SLOTS;
+            mbar_arrive_expect_tx(mfull(ms), MT_SLOT);
+            tma_load_2d(sM + ms * MT_SLOT, &tm_m, kt, (int)r0, mfull(ms));
+          }
+          mbar_arrive_expect_tx(full(s), V_BYTES);
           tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
         }
         if (!MT) {
@@ -229,6 +248,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) {
         const int first = issued > STAGES ? issued - STAGES : 0;
         for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
+        if (MT && issued > 0) {  // the mask boxes still in flight
+          const int nbox = (issued + MW - 1) / MW;
+          const int b0 = nbox > L::MT_SLOTS ? nbox - L::MT_SLOTS : 0;
+          for (int b = b0; b < nbox; ++b) mbar_wait(mfull(b % L::MT_SLOTS), (b / L::MT_SLOTS) & 1);
+        }
       }
     }
     __syncwarp();
@@ -268,16 +292,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---- densify, then epilogue -----------------------------------------
     const int dw = warp - FIRST_DENSIFY_WARP;
+    const int grp = dw / WPG, wg = dw % WPG;
     bool ok = true;
-    for (int kt = 0; kt < words; ++kt) {
+    int box = -1;  // mask box this warp last waited for
+    for (int kt = grp; kt < words; kt += DG) {
       const int s = kt % STAGES, u = kt / STAGES;
+      bool got = mbar_wait(full(s), u & 1);
+      if (MT && kt / MW != box) {
+        // The box's slot is refilled only after the MMAs of a later stage, so
+        // after every group is done with it: its phase here is this box's.
+        box = kt / MW;
+        got = got && mbar_wait(mfull(box % L::MT_SLOTS), (box / L::MT_SLOTS) & 1);
+      }
       // The warp decides together, so no lane is left behind at a warp barrier.
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full(s), u & 1))) { ok = false; break; }
-      // With MT the stage's masks came with stage MW * (kt / MW), whose full
-      // barrier this warp has already seen complete (stages are consumed in order).
+      if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
       const uint32_t sMw = MT ? sM + ((kt / MW) % L::MT_SLOTS) * MT_SLOT + (kt % MW) * 4u
                               : sM + s * M_BYTES;
-      densify_stage(sA + s * A_BYTES, sV + s * V_BYTES, sMw, MT ? MW * 4u : 4u, dw, lane);
+      densify_stage<RPW>(sA + s * A_BYTES, sV + s * V_BYTES, sMw, MT ? MW * 4u : 4u, wg, lane);
       // Each lane orders its tile writes before the tensor core's reads; the
       // warp barrier then lets one release-arrive publish all 32 lanes' writes
       // (one arrival per warp: 32 arrivals on one barrier word serialise).
@@ -291,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (__all_sync(0xFFFFFFFFu, ok)) {
       const int quad = warp & 3;              // TMEM lanes 32*quad .. +31
       const int qi = dw >> 2;                 // this warp's index among its quadrant's warps
-      constexpr int QW = DENSIFY_WARPS / 4;   // warps per quadrant, striding the columns
+      constexpr int QW = DW / 4;              // warps per quadrant, striding the columns
       const int64_t r = r0 + 32 * quad + lane;
       const bool row_ok = r < rows;
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * quad) << 16);
@@ -321,10 +352,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---- host ------------------------------------------------------------------
 struct Variant {
-  int nmma, nb, stages, g;
+  int nmma, nb, stages, g, dg, dw;
 };
-constexpr Variant kVariants[] = {
-    {256, 2, 4, 1}, {256, 1, 6, 1}, {128, 1, 8, 2}, {64, 1, 8, 2}, {256, 2, 5, 1}};
+constexpr Variant kVariants[] = {{256, 2, 4, 1, 2, 16}, {256, 1, 6, 1, 2, 16}, {128, 1, 8, 1, 4, 16},
+                                 {64, 1, 8, 1, 4, 16},  {256, 2, 5, 1, 4, 16}};
 constexpr int kVariantCount = sizeof(kVariants) / sizeof(kVariants[0]);
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -360,7 +391,7 @@ static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMMA, int NB, int STAGES, int G, bool MT>
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW, bool MT>
 static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
   using L = Layout<NMMA, NB, STAGES, MT>;
   CUtensorMap tm_v, tm_x, tm_m;
@@ -374,7 +405,7 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
       !encode_2d(&tm_x, p.X, (uint64_t)p.words * 32, (uint64_t)p.T, (uint64_t)p.ldx * 2, BK,
                  NMMA, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, G, MT>;
+  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, G, DG, DW, MT>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -386,7 +417,7 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
   const dim3 grid((unsigned)((p.T + L::BN - 1) / L::BN), (unsigned)((p.rows + BM - 1) / BM));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(threads_for(DW));
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, k, tm_v, tm_x, tm_m, p.masks, p.Y, p.rows, p.words, p.T,
@@ -395,25 +426,40 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
 
 // Mask words by TMA when the mask array allows it (16-byte aligned, row pitch
 // words * 4 a multiple of 16: every decoder shape), else by cp.async.
-template <int NMMA, int NB, int STAGES, int G>
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW>
 static cudaError_t launch_tc(const SpmmTcParams& p, cudaStream_t stream) {
   const bool mt = p.words % 4 == 0 && (reinterpret_cast<uintptr_t>(p.masks) & 15) == 0;
-  return mt ? launch_tc_mt<NMMA, NB, STAGES, G, true>(p, stream)
-            : launch_tc_mt<NMMA, NB, STAGES, G, false>(p, stream);
+  return mt ? launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, true>(p, stream)
+            : launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, false>(p, stream);
 }
 
 }  // namespace tc
 
 int spmm_tc_variant_count() { return tc::kVariantCount; }
 
-// Measured on GB300 (70B- and 8B-shaped decoder matrices): 512 tokens per
-// block with 5 stages is fastest from T = 512 up; at T = 256 one 256-token
-// N-part; below, the 128- and 64-token blocks waste the least of the MMA.
-int spmm_tc_default_variant(int64_t T) {
-  if (T > 256) return 4;
-  if (T > 128) return 1;
-  if (T > 64) return 2;
-  return 3;
+// The variant that minimises (waves of blocks) x (time of one block), with
+// each variant's time per 32-column stage measured on GB300 over the
+// decoder-layer shapes (ns, one block per SM): 512 tokens 453 (5 stages),
+// 256 tokens 352, 128 tokens 288, 64 tokens 279.  A larger token tile does
+// more work per stage, a smaller one fills more SMs when rows are few.
+int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
+  static const struct {
+    int variant, tokens;
+    double ns_per_stage;
+  } cand[] = {{4, 512, 453.0}, {1, 256, 352.0}, {2, 128, 288.0}, {3, 64, 279.0}};
+  if (sms < 1) sms = 1;
+  const int64_t row_tiles = (rows + 127) / 128;
+  int best = 3;
+  double best_t = 0.0;
+  for (const auto& c : cand) {
+    const int64_t blocks = row_tiles * ((T + c.tokens - 1) / c.tokens);
+    const double t = (double)((blocks + sms - 1) / sms) * c.ns_per_stage;
+    if (best_t == 0.0 || t < best_t * 0.97) {  // prefer the earlier (larger) tile on near-ties
+      best = c.variant;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 int spmm_tc_block_tokens(int variant) {
@@ -422,11 +468,11 @@ int spmm_tc_block_tokens(int variant) {
 
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
   switch (variant) {
-    case 0: return tc::launch_tc<256, 2, 4, 1>(p, stream);
-    case 1: return tc::launch_tc<256, 1, 6, 1>(p, stream);
-    case 2: return tc::launch_tc<128, 1, 8, 2>(p, stream);
-    case 3: return tc::launch_tc<64, 1, 8, 2>(p, stream);
-    case 4: return tc::launch_tc<256, 2, 5, 1>(p, stream);
+    case 0: return tc::launch_tc<256, 2, 4, 1, 2, 16>(p, stream);
+    case 1: return tc::launch_tc<256, 1, 6, 1, 2, 16>(p, stream);
+    case 2: return tc::launch_tc<128, 1, 8, 1, 4, 16>(p, stream);
+    case 3: return tc::launch_tc<64, 1, 8, 1, 4, 16>(p, stream);
+    case 4: return tc::launch_tc<256, 2, 5, 1, 4, 16>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

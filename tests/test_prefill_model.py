@@ -23,6 +23,7 @@ A_BYTES, V_BYTES, M_BYTES = BM * ROW_BYTES, BM * 32, BM * 4
 DENSIFY_WARPS = 16
 ROWS_PER_WARP = BM // DENSIFY_WARPS
 VARIANTS = [(256, 2, 4), (256, 1, 6), (128, 1, 8), (64, 1, 8), (256, 2, 5)]
+DENSIFY_GROUPS = [2, 2, 4, 4, 4]   # stage-parallel densify groups per variant
 SMEM_OPTIN = 232448  # bytes of dynamic shared memory a GB300 block may opt into
 
 
@@ -58,7 +59,7 @@ def layout(nmma, nb, stages, mt=True):
     v_off = b_off + stages * bn * ROW_BYTES
     m_off = v_off + stages * V_BYTES
     bar_off = m_off + (mt_slots(stages) * MT_SLOT if mt else stages * M_BYTES)
-    slot_off = bar_off + (3 * stages + 1) * 8
+    slot_off = bar_off + (3 * stages + 1 + mt_slots(stages)) * 8
     return dict(BN=bn, B_OFF=b_off, V_OFF=v_off, M_OFF=m_off, BAR_OFF=bar_off,
                 BYTES=slot_off + 16, SMEM=slot_off + 16 + 1024)
 
@@ -70,19 +71,20 @@ def tma_sw64(r, byte_in_row):
     return L ^ (((L >> 7) & 3) << 4)
 
 
-def densify(masks_row_words, values_rows, sV=0, sM=None):
-    """Run the kernel's densify_stage on one stage; returns {phys byte: u32}
-    and the list of shared-memory byte addresses it read."""
+def densify(masks_row_words, values_rows, rpw=ROWS_PER_WARP):
+    """Run the kernel's densify_stage<rpw> for one stage over the warps of one
+    densify group (128 / rpw warps); returns {phys byte: u32} and the list of
+    shared-memory byte addresses it read."""
     writes, reads = {}, []
-    for dw in range(DENSIFY_WARPS):
+    for dw in range(BM // rpw):
         for lane in range(32):
             h, p = lane >> 4, lane & 15
             b0 = 2 * p
             below = (1 << b0) - 1
             col_byte = (p & 3) * 4
             chunk = p >> 2
-            for i in range(ROWS_PER_WARP // 2):
-                r = dw * ROWS_PER_WARP + 2 * i + h
+            for i in range(rpw // 2):
+                r = dw * rpw + 2 * i + h
                 m = int(masks_row_words[r])
                 reads.append(("M", 4 * r, r, 1))
                 c = popc(m & below)
@@ -114,8 +116,9 @@ def random_masks(rng, rows, N, M):
     return words
 
 
+@pytest.mark.parametrize("rpw", [8, 16, 32])
 @pytest.mark.parametrize("N,M", [(2, 4), (4, 8), (8, 16), (16, 32)])
-def test_densify_equals_unpack_and_matches_tma_swizzle(N, M):
+def test_densify_equals_unpack_and_matches_tma_swizzle(N, M, rpw):
     rng = np.random.default_rng(N)
     masks = random_masks(rng, BM, N, M)
     vals = rng.integers(1, 0x7BFF, size=(BM, 16), dtype=np.int64)   # nonzero fp16 bit patterns
@@ -123,7 +126,7 @@ def test_densify_equals_unpack_and_matches_tma_swizzle(N, M):
     for r in range(BM):
         for k in range(16):
             values_rows[32 * r + 2 * k] = int(vals[r, k])
-    writes, reads = densify(masks, values_rows)
+    writes, reads = densify(masks, values_rows, rpw)
     assert len(writes) == BM * 16          # every (row, column pair) exactly once
     for phys, (out, r, col) in writes.items():
         assert phys == tma_sw64(r, 2 * col)
@@ -158,6 +161,24 @@ def test_corrupt_masks_read_inside_the_allocation():
             L = layout(nmma, nb, stages, mt)
             last_stage_v = L["V_OFF"] + (stages - 1) * V_BYTES
             assert last_stage_v + vmax + 2 <= L["BYTES"]
+
+
+def test_densify_groups_split_stages_and_read_every_mask_box():
+    """Group g of DG takes stages g, g + DG, ...: every stage exactly once,
+    each group in increasing order, and (DG <= MW) every group touches every
+    box of MW stages -- the condition under which a warp's wait on a mask
+    box's barrier always sees that box's phase."""
+    for dg in set(DENSIFY_GROUPS):
+        assert DENSIFY_WARPS % dg == 0 and (BM // (DENSIFY_WARPS // dg)) % 8 == 0
+        words = 37
+        seen = []
+        for g in range(dg):
+            mine = list(range(g, words, dg))
+            assert mine == sorted(mine)
+            seen += mine
+            boxes = sorted({k // MW for k in mine})
+            assert boxes == list(range(boxes[-1] + 1))  # no box skipped
+        assert sorted(seen) == list(range(words))
 
 
 def test_mask_slots_are_not_refilled_before_their_last_reader():
