@@ -108,6 +108,11 @@ __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t
   const uint32_t col_byte = (uint32_t)(p & 3) * 4u;
   const uint32_t chunk = (uint32_t)(p >> 2);
   const uint32_t r_first = (uint32_t)(wg * RPW + h);
+  // prmt selectors by q (bit 0: column 2p kept, bit 1: 2p+1 kept) for the
+  // values v0 (rank c) and v1 (rank c + 1), loaded zero-extended so bytes 2-3
+  // and 6-7 are zero: q 0 -> 0x3232 (0, 0), 1 -> 0x3210 (v0, 0),
+  // 2 -> 0x1032 (0, v0), 3 -> 0x5410 (v0, v1).
+  constexpr uint32_t kSelLo = 0x32103232u, kSelHi = 0x54101032u;
   uint32_t m[R], q[R], v0[R], v1[R];
 #pragma unroll
   for (int i = 0; i < R; ++i) m[i] = lds_u32(sMw + mstride * (r_first + 2 * i));
@@ -115,18 +120,15 @@ __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t
   for (int i = 0; i < R; ++i) {
     const uint32_t r = r_first + 2 * i;
     const uint32_t c = __popc(m[i] & below);     // rank of column 2p among kept columns
-    q[i] = (m[i] >> b0) & 3u;                    // bit 0: column 2p kept, bit 1: 2p+1 kept
+    q[i] = (m[i] >> b0) & 3u;
     const uint32_t a0 = sV + 32u * r + 2u * c;
     v0[i] = lds_u16_32(a0);
-    v1[i] = lds_u16_32(a0 + ((q[i] & 1u) << 1));
+    v1[i] = lds_u16_32(a0 + 2u);
   }
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const uint32_t r = r_first + 2 * i;
-    // byte k of keep = 0xFF when its column is kept: sign-replicate bytes 0/1
-    // of q * 0x4080 (bit 7 <- column 2p, bit 15 <- column 2p+1).
-    const uint32_t keep = prmt(q[i] * 0x4080u, 0u, 0x9988u);
-    const uint32_t out = prmt(v0[i], v1[i], 0x5410u) & keep;
+    const uint32_t out = prmt(v0[i], v1[i], prmt(kSelLo, kSelHi, q[i] * 0x22u + 0x10u));
     // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3, and
     // (r >> 1) & 3 == i & 3 because wg * RPW is a multiple of 8.
     const uint32_t phys = r * ROW_BYTES + ((chunk ^ (uint32_t)(i & 3)) << 4) + col_byte;

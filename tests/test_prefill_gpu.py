@@ -162,3 +162,26 @@ def test_prefill_full_size_sampled(nm, orc, rows, cols, T, pat):
         y_ref, s = orc.spmv_rows_f64(hv, hm, cols, X[t], row_ids)
         got = f16_to_f64(Yh[t, row_ids])
         assert np.all(np.abs(got - y_ref) <= oracle.tolerance(s)), f"token {t}"
+
+
+def test_prefill_nonfinite_activation_is_dense_semantics(nm, orc):
+    """Pruned weights enter the MMA as +0: an infinite X[t][c] makes every row
+    that prunes column c NaN (0 * inf) and every row that keeps it +-inf (the
+    sign of its weight); the other tokens are untouched."""
+    rows, cols, T = 256, 1024, 64
+    W, X = gen(rows, cols, T, 11)
+    t_bad, c_bad = 5, 100
+    X[t_bad, c_bad] = np.uint16(0x7C00)   # +inf
+    ov, om, v, m = dev_packed(orc, W, 2, 4)
+    Y = f16_to_f64(from_dev(nm.nm_spmm_prefill(v, m, to_dev(X))))
+    kept = ((om[:, c_bad // 32] >> np.uint32(c_bad % 32)) & 1).astype(bool)
+    Wp = f16_to_f64(orc.unpack(ov, om, cols))
+    assert kept.any() and (~kept).any()
+    assert np.isnan(Y[t_bad][~kept]).all()
+    assert np.array_equal(np.sign(Y[t_bad][kept]), np.sign(Wp[kept, c_bad]))
+    assert np.isinf(Y[t_bad][kept]).all()
+    for t in range(T):
+        if t == t_bad:
+            continue
+        y_ref, s = orc.spmv_f64(ov, om, cols, X[t])
+        assert np.all(np.abs(Y[t] - y_ref) <= oracle.tolerance(s)), f"token {t}"

@@ -41,6 +41,10 @@ def prmt(a, b, sel):
     return out
 
 
+# prmt selectors by q: 0 -> (0, 0), 1 -> (v0, 0), 2 -> (0, v0), 3 -> (v0, v1)
+SEL_LO, SEL_HI = 0x32103232, 0x54101032
+
+
 def popc(v):
     return bin(v & 0xFFFFFFFF).count("1")
 
@@ -90,13 +94,12 @@ def densify(masks_row_words, values_rows, rpw=ROWS_PER_WARP):
                 c = popc(m & below)
                 q = (m >> b0) & 3
                 a0 = 32 * r + 2 * c
-                a1 = a0 + ((q & 1) << 1)
-                reads.append(("V", a0, r, q & 1))
-                reads.append(("V", a1, r, (q >> 1) & 1))
-                v0 = values_rows.get(a0, 0)
-                v1 = values_rows.get(a1, 0)
-                keep = prmt((q * 0x4080) & 0xFFFFFFFF, 0, 0x9988)
-                out = prmt(v0, v1, 0x5410) & keep
+                reads.append(("V", a0, r, int(q != 0)))        # rank c: used unless both absent
+                reads.append(("V", a0 + 2, r, int(q == 3)))    # rank c + 1: used when both kept
+                v0 = values_rows.get(a0, 0)                     # zero-extended 16-bit loads
+                v1 = values_rows.get(a0 + 2, 0)
+                sel = prmt(SEL_LO, SEL_HI, q * 0x22 + 0x10)
+                out = prmt(v0, v1, sel)
                 phys = r * ROW_BYTES + ((chunk ^ (i & 3)) << 4) + col_byte
                 assert phys not in writes, "element written twice"
                 writes[phys] = (out, r, 2 * p)
@@ -142,9 +145,9 @@ def test_densify_equals_unpack_and_matches_tma_swizzle(N, M, rpw):
         elif used:
             assert 32 * r <= addr < 32 * r + 32        # a kept value comes from its own row
         else:
-            # an absent column's load (result masked to +0) may sit one value
-            # past the row when every kept bit lies left of it: rank 16
-            assert 32 * r <= addr <= 32 * r + 32
+            # a load whose value is not selected may sit up to two values past
+            # the row (rank 16 when every kept bit lies left of the pair, + 1)
+            assert 32 * r <= addr <= 32 * r + 34
 
 
 def test_corrupt_masks_read_inside_the_allocation():
