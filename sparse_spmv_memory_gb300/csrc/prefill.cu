@@ -16,13 +16,15 @@
 //    so that the two run side by side: warp 0 loads the token tile of X by
 //    TMA (BN x 32 fp16, 64-byte swizzle); warp 2 loads the tile's compact
 //    values (128 rows x 16 fp16) by TMA and its mask words (by TMA, four
-//    stages per box, when the mask pitch allows it, else by cp.async).  Both
-//    complete on the stage's "full" mbarrier.
-//  * Warps 3..18 (densify): expand each row's 16 kept values into the 32
-//    columns of a K-major, 64-byte-swizzled fp16 tile in shared memory, the
-//    layout the MMA descriptor names.  A lane builds two adjacent columns:
-//    the rank of its first column among the word's set bits (one popc) is the
-//    index of its value in the compact row; absent columns become +0.
+//    stages per box on a barrier of the box's own, when the mask pitch allows
+//    it, else by cp.async).  Values and X complete on the stage's "full"
+//    mbarrier.
+//  * Warps 3..18 (densify), in DG groups that take alternate stages: expand
+//    each row's 16 kept values into the 32 columns of a K-major,
+//    64-byte-swizzled fp16 tile in shared memory, the layout the MMA
+//    descriptor names.  A lane builds two adjacent columns: the rank of its
+//    first column among the word's set bits (one popc) indexes its value in
+//    the compact row; one table-driven prmt places it, its neighbour or zeros.
 //  * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (M = 128,
 //    N = NMMA, K = 16; two per stage and N-part) on the densified tile and the
 //    X tile, and tcgen05.commit frees the stage when those MMAs are done.
@@ -260,13 +262,12 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issuer ----------------------------------------------------
-    // Waits only on the densify barriers, and on one per G stages: each
-    // densify warp saw the stage's "full" barrier complete (so the TMA-loaded
-    // X tile is visible through its release-arrive) and arrives on the stages
-    // in order, so afull(kt + G - 1) complete implies the earlier ones are.
-    // A barrier test costs the single issuing thread a few hundred cycles,
-    // a whole stage's budget when N is small (G = 2 there); with large N the
-    // wait for a second stage would delay the first stage's MMAs (G = 1).
+    // Waits only on the densify barriers: the densify warps saw the stage's
+    // "full" barrier complete (so the TMA-loaded X tile is visible through
+    // their release-arrive).  With one densify group (DG == 1) every warp
+    // arrives on the stages in order, so G = 2 may wait on every second
+    // barrier only (afull(kt + 1) complete implies afull(kt)); with several
+    // groups each stage's barrier is waited on (G = 1).
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
       for (int kt = 0; kt < words; kt += G) {
