@@ -168,7 +168,9 @@ int nm_spmv_swiglu_ex(const void *values, const uint32_t *masks, int64_t rows, i
  * Same arithmetic, rounding, determinism and structural-zero rule as nm_spmv
  * (a non-finite activation of token j reaches only column j of Y); each column of Y is
  * within the same tolerance of the exact product (and equals nm_spmv's
- * result whenever the sums are exact).  batch outside 1..8 -> NM_ERR_SHAPE;
+ * result whenever the sums are exact).  nm_spmm with batch > 8 is served by
+ * nm_spmm_prefill (tensor cores; workspace ignored; its numerics); nm_spmm_ex
+ * and the workspace queries take batch 1..8 only.  batch < 1 -> NM_ERR_SHAPE;
  * a short workspace -> NM_ERR_WORKSPACE.  Y must not overlap any input or the
  * workspace.
  * ------------------------------------------------------------------------- */

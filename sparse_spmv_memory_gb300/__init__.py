@@ -264,10 +264,11 @@ def nm_spmm_variant_count() -> int:
 
 def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int = -1,
             grid: int = 0, slices: int = 0, flags: int | None = None, cols: int | None = None):
-    """Y = W X for a batch of 1..8 tokens: X fp16 [batch][ldx] (first ``cols``
-    columns used), Y fp16 [batch][ldy].  A workspace of
-    nm_spmm_workspace_bytes(...) bytes is allocated with PyTorch when needed
-    and none is given."""
+    """Y = W X for a batch of tokens: X fp16 [batch][ldx] (first ``cols``
+    columns used), Y fp16 [batch][ldy].  Batches of 1..8 run on the CUDA
+    cores (a workspace of nm_spmm_workspace_bytes(...) bytes is allocated
+    with PyTorch when needed and none is given); larger ones on the tensor
+    cores (nm_spmm_prefill)."""
     torch = _torch()
     _need_cuda(values, masks, X)
     rows = masks.shape[0]
@@ -279,7 +280,7 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
         Y = torch.empty((batch, rows), dtype=torch.float16, device=X.device)
     _need_cuda(Y, workspace)
     L = lib()
-    if workspace is None:
+    if workspace is None and batch <= 8:
         need = L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, slices)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=X.device)

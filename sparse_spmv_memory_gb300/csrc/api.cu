@@ -204,6 +204,8 @@ size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int var
 int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
                size_t workspace_bytes, int variant, int grid, int slices, int flags, void* stream);
+int nm_spmm_prefill(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                    const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, void* stream);
 
 const char* nm_status_string(int status) {
   switch (status) {
@@ -456,6 +458,8 @@ int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
 int nm_spmm(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* X,
             int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace, size_t workspace_bytes,
             void* stream) {
+  if (batch > 8)  // beyond the CUDA-core kernel's batch: the tensor-core path, no workspace
+    return nm_spmm_prefill(values, masks, rows, cols, X, ldx, batch, Y, ldy, stream);
   return nm_spmm_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace, workspace_bytes,
                     -1, 0, 0, NM_FLAG_PDL, stream);
 }

@@ -94,47 +94,57 @@ struct Layout {
 };
 
 // RPW rows x 32 columns of one stage: lane (h, p) of warp wg builds columns
-// 2p, 2p+1 of rows r_i = wg * RPW + 2 i + h, i < RPW / 2.  The shared-memory
-// accesses are issued in three batches (mask words, values, stores) so that
-// each batch's latency is paid once per stage rather than once per row.
+// 4p .. 4p+3 of rows r_i = wg * RPW + 4 i + h (h = lane / 8, p = lane % 8),
+// i < RPW / 4, as two column pairs.  For a pair (2j, 2j+1) of the row's word
+// the rank c of column 2j among the set bits indexes its value in the compact
+// row; the values of rank c and c + 1 are loaded zero-extended and one prmt,
+// its selector looked up from a 4-entry table by the pair's two mask bits,
+// places them or zeros.  The shared-memory accesses are issued in three
+// batches (mask words, values, stores) so that each batch's latency is paid
+// once per stage rather than once per row.
 // sMw: this stage's mask word of row 0; mstride: bytes from one row's word
 // to the next row's.
 template <int RPW>
 __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t sMw,
                                               uint32_t mstride, int wg, int lane) {
-  static_assert(RPW % 8 == 0, "the swizzle phase below needs whole groups of 8 rows");
-  constexpr int R = RPW / 2;
-  const int h = lane >> 4, p = lane & 15;
-  const uint32_t b0 = 2u * p;
-  const uint32_t below = (1u << b0) - 1u;       // columns of the word left of 2p
-  const uint32_t col_byte = (uint32_t)(p & 3) * 4u;
-  const uint32_t chunk = (uint32_t)(p >> 2);
+  static_assert(RPW % 8 == 0, "the swizzle phases below need whole groups of 8 rows");
+  constexpr int R = RPW / 4;
+  const int h = lane >> 3, p = lane & 7;
+  const uint32_t b0 = 4u * p;
+  const uint32_t below = (1u << b0) - 1u;       // columns of the word left of 4p
   const uint32_t r_first = (uint32_t)(wg * RPW + h);
-  // prmt selectors by q (bit 0: column 2p kept, bit 1: 2p+1 kept) for the
-  // values v0 (rank c) and v1 (rank c + 1), loaded zero-extended so bytes 2-3
-  // and 6-7 are zero: q 0 -> 0x3232 (0, 0), 1 -> 0x3210 (v0, 0),
-  // 2 -> 0x1032 (0, v0), 3 -> 0x5410 (v0, v1).
+  // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3.  Row r_i gives
+  // (r_i >> 1) & 3 = (2 i + (h >> 1)) & 3 = (2 i & 3) ^ (h >> 1), since
+  // wg * RPW / 2 is a multiple of 4: two lane-constant offsets by i & 1.
+  const uint32_t lane_chunk = (uint32_t)((p >> 1) ^ (h >> 1));
+  const uint32_t in_chunk = (uint32_t)(p & 1) * 8u;
+  const uint32_t off_even = (lane_chunk << 4) + in_chunk;           // i even: phase ^ 0
+  const uint32_t off_odd = ((lane_chunk ^ 2u) << 4) + in_chunk;     // i odd:  phase ^ 2
+  // prmt selectors by q (bit 0: column 2j kept, bit 1: 2j+1 kept) for the
+  // values v (rank c) and w (rank c + 1): q 0 -> 0x3232 (0, 0),
+  // 1 -> 0x3210 (v, 0), 2 -> 0x1032 (0, v), 3 -> 0x5410 (v, w).
   constexpr uint32_t kSelLo = 0x32103232u, kSelHi = 0x54101032u;
-  uint32_t m[R], q[R], v0[R], v1[R];
+  uint32_t m[R], nib[R], v[R][4];
 #pragma unroll
-  for (int i = 0; i < R; ++i) m[i] = lds_u32(sMw + mstride * (r_first + 2 * i));
+  for (int i = 0; i < R; ++i) m[i] = lds_u32(sMw + mstride * (r_first + 4 * i));
 #pragma unroll
   for (int i = 0; i < R; ++i) {
-    const uint32_t r = r_first + 2 * i;
-    const uint32_t c = __popc(m[i] & below);     // rank of column 2p among kept columns
-    q[i] = (m[i] >> b0) & 3u;
-    const uint32_t a0 = sV + 32u * r + 2u * c;
-    v0[i] = lds_u16_32(a0);
-    v1[i] = lds_u16_32(a0 + 2u);
+    const uint32_t r = r_first + 4 * i;
+    const uint32_t c = __popc(m[i] & below);            // rank of column 4p
+    nib[i] = (m[i] >> b0) & 15u;
+    const uint32_t c2 = c + __popc(nib[i] & 3u);         // rank of column 4p + 2
+    const uint32_t a0 = sV + 32u * r + 2u * c, a2 = sV + 32u * r + 2u * c2;
+    v[i][0] = lds_u16_32(a0);
+    v[i][1] = lds_u16_32(a0 + 2u);
+    v[i][2] = lds_u16_32(a2);
+    v[i][3] = lds_u16_32(a2 + 2u);
   }
 #pragma unroll
   for (int i = 0; i < R; ++i) {
-    const uint32_t r = r_first + 2 * i;
-    const uint32_t out = prmt(v0[i], v1[i], prmt(kSelLo, kSelHi, q[i] * 0x22u + 0x10u));
-    // 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3, and
-    // (r >> 1) & 3 == i & 3 because wg * RPW is a multiple of 8.
-    const uint32_t phys = r * ROW_BYTES + ((chunk ^ (uint32_t)(i & 3)) << 4) + col_byte;
-    sts_u32(sA + phys, out);
+    const uint32_t r = r_first + 4 * i;
+    const uint32_t lo = prmt(v[i][0], v[i][1], prmt(kSelLo, kSelHi, (nib[i] & 3u) * 0x22u + 0x10u));
+    const uint32_t hi = prmt(v[i][2], v[i][3], prmt(kSelLo, kSelHi, (nib[i] >> 2) * 0x22u + 0x10u));
+    sts_u64(sA + r * ROW_BYTES + ((i & 1) ? off_odd : off_even), lo, hi);
   }
 }
 

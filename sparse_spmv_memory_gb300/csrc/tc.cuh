@@ -219,6 +219,10 @@ __device__ __forceinline__ uint32_t lds_u16_32(uint32_t saddr) {
   return v;
 }
 
+__device__ __forceinline__ void sts_u64(uint32_t saddr, uint32_t lo, uint32_t hi) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(saddr), "r"(lo), "r"(hi) : "memory");
+}
+
 __device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }

@@ -185,3 +185,16 @@ def test_prefill_nonfinite_activation_is_dense_semantics(nm, orc):
             continue
         y_ref, s = orc.spmv_f64(ov, om, cols, X[t])
         assert np.all(np.abs(Y[t] - y_ref) <= oracle.tolerance(s)), f"token {t}"
+
+
+def test_nm_spmm_beyond_eight_tokens_takes_the_tensor_core_path(nm, orc):
+    """nm_spmm with batch > 8 is served by nm_spmm_prefill: the same bits."""
+    rows, cols, T = 300, 2048, 12
+    W, X = gen(rows, cols, T, 12)
+    ov, om, v, m = dev_packed(orc, W, 8, 16)
+    Xd = to_dev(X)
+    a = from_dev(nm.nm_spmm(v, m, Xd))
+    b = from_dev(nm.nm_spmm_prefill(v, m, Xd))
+    assert np.array_equal(a, b)
+    y_ref, s = oracle_Y(orc, ov, om, cols, X)
+    assert np.all(np.abs(f16_to_f64(a) - y_ref) <= oracle.tolerance(s))

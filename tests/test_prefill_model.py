@@ -77,32 +77,37 @@ def tma_sw64(r, byte_in_row):
 
 def densify(masks_row_words, values_rows, rpw=ROWS_PER_WARP):
     """Run the kernel's densify_stage<rpw> for one stage over the warps of one
-    densify group (128 / rpw warps); returns {phys byte: u32} and the list of
-    shared-memory byte addresses it read."""
+    densify group (128 / rpw warps); returns {phys byte: (u32, row, column)}
+    and the list of shared-memory reads (kind, address, row, used)."""
     writes, reads = {}, []
     for dw in range(BM // rpw):
         for lane in range(32):
-            h, p = lane >> 4, lane & 15
-            b0 = 2 * p
+            h, p = lane >> 3, lane & 7
+            b0 = 4 * p
             below = (1 << b0) - 1
-            col_byte = (p & 3) * 4
-            chunk = p >> 2
-            for i in range(rpw // 2):
-                r = dw * rpw + 2 * i + h
+            lane_chunk = (p >> 1) ^ (h >> 1)
+            in_chunk = (p & 1) * 8
+            off_even = (lane_chunk << 4) + in_chunk
+            off_odd = ((lane_chunk ^ 2) << 4) + in_chunk
+            for i in range(rpw // 4):
+                r = dw * rpw + 4 * i + h
                 m = int(masks_row_words[r])
                 reads.append(("M", 4 * r, r, 1))
                 c = popc(m & below)
-                q = (m >> b0) & 3
-                a0 = 32 * r + 2 * c
-                reads.append(("V", a0, r, int(q != 0)))        # rank c: used unless both absent
-                reads.append(("V", a0 + 2, r, int(q == 3)))    # rank c + 1: used when both kept
-                v0 = values_rows.get(a0, 0)                     # zero-extended 16-bit loads
-                v1 = values_rows.get(a0 + 2, 0)
-                sel = prmt(SEL_LO, SEL_HI, q * 0x22 + 0x10)
-                out = prmt(v0, v1, sel)
-                phys = r * ROW_BYTES + ((chunk ^ (i & 3)) << 4) + col_byte
-                assert phys not in writes, "element written twice"
-                writes[phys] = (out, r, 2 * p)
+                nib = (m >> b0) & 15
+                c2 = c + popc(nib & 3)
+                a0, a2 = 32 * r + 2 * c, 32 * r + 2 * c2
+                q_lo, q_hi = nib & 3, nib >> 2
+                reads += [("V", a0, r, int(q_lo != 0)), ("V", a0 + 2, r, int(q_lo == 3)),
+                          ("V", a2, r, int(q_hi != 0)), ("V", a2 + 2, r, int(q_hi == 3))]
+                lo = prmt(values_rows.get(a0, 0), values_rows.get(a0 + 2, 0),
+                          prmt(SEL_LO, SEL_HI, q_lo * 0x22 + 0x10))
+                hi = prmt(values_rows.get(a2, 0), values_rows.get(a2 + 2, 0),
+                          prmt(SEL_LO, SEL_HI, q_hi * 0x22 + 0x10))
+                phys = r * ROW_BYTES + (off_odd if i & 1 else off_even)
+                for off, val, col in ((0, lo, 4 * p), (4, hi, 4 * p + 2)):
+                    assert phys + off not in writes, "element written twice"
+                    writes[phys + off] = (val, r, col)
     return writes, reads
 
 
