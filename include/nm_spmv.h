@@ -281,6 +281,17 @@ int nm_spmm_prefill_variant_count(void);
  * Host-synchronous (reads a device counter); negative nm_status on error. */
 int64_t nm_wait_timeouts(int reset);
 
+/* nm_prefill_stall_selftest -- exercises the bounded-wait path of the
+ * prefill kernel (self-test; no counterpart on the pages): launches it on the
+ * given buffers (as for nm_spmm_prefill, 64-token variant) with its weight
+ * producer disabled, so that no stage ever completes, and every wait limited
+ * to wait_limit_us (1..2,000,000).  Each role's wait then runs out, is counted
+ * in nm_wait_timeouts(), and the kernel returns without storing Y; the device
+ * stays usable.  Asynchronous; NM_OK once launched. */
+int nm_prefill_stall_selftest(const void *values, const uint32_t *masks, int64_t rows,
+                              int64_t cols, const void *X, int64_t ldx, int64_t T, void *Y,
+                              int64_t ldy, int64_t wait_limit_us, void *stream);
+
 /* ---------------------------------------------------------------------------
  * nm_check_masks_noalloc -- the same count as nm_check_masks, without any
  * device allocation.  The paper has no counterpart to this entry point; it

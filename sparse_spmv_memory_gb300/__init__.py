@@ -28,6 +28,7 @@ __all__ = [
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
     "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
     "nm_spmv_swiglu", "nm_spmm_prefill", "nm_spmm_prefill_variant_count", "nm_wait_timeouts",
+    "nm_prefill_stall_selftest",
 ]
 
 NM_OK = 0
@@ -93,6 +94,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_spmm_prefill_ex": ([P, P, I64, I64, P, I64, I64, P, I64, I32, P], I32),
         "nm_spmm_prefill_variant_count": ([], I32),
         "nm_wait_timeouts": ([I32], I64),
+        "nm_prefill_stall_selftest": ([P, P, I64, I64, P, I64, I64, P, I64, I64, P], I32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -323,6 +325,17 @@ def nm_spmm_prefill(values, masks, X, Y=None, stream=None, variant: int = -1,
                                   _ptr(Y), Y.stride(0), variant, _stream(stream))
     _check(st, "nm_spmm_prefill")
     return Y
+
+
+def nm_prefill_stall_selftest(values, masks, X, Y, wait_limit_us: int, stream=None):
+    """Launch the prefill kernel with its weight producer disabled (every
+    bounded wait runs out; Y is left untouched).  Self-test of the wait path."""
+    _need_cuda(values, masks, X, Y)
+    T, ldx = X.shape
+    _check(lib().nm_prefill_stall_selftest(_ptr(values), _ptr(masks), masks.shape[0], ldx,
+                                           _ptr(X), X.stride(0), T, _ptr(Y), Y.stride(0),
+                                           int(wait_limit_us), _stream(stream)),
+           "nm_prefill_stall_selftest")
 
 
 def nm_wait_timeouts(reset: bool = False) -> int:

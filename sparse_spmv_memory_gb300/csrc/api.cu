@@ -507,6 +507,33 @@ int nm_spmm_prefill(const void* values, const uint32_t* masks, int64_t rows, int
   return nm_spmm_prefill_ex(values, masks, rows, cols, X, ldx, T, Y, ldy, -1, stream);
 }
 
+int nm_prefill_stall_selftest(const void* values, const uint32_t* masks, int64_t rows,
+                              int64_t cols, const void* X, int64_t ldx, int64_t T, void* Y,
+                              int64_t ldy, int64_t wait_limit_us, void* stream) {
+  if (!values || !masks || !X || !Y) return NM_ERR_NULL;
+  if (rows <= 0 || rows >= kMaxRows || (rows + 127) / 128 > 65535 || cols <= 0 || cols % 32 != 0 ||
+      T <= 0 || T >= kMaxRows || ldx < cols || ldy < rows || wait_limit_us <= 0 ||
+      wait_limit_us > 2000000)
+    return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
+      !aligned(Y, 2))
+    return NM_ERR_ALIGN;
+  SpmmTcParams p;
+  p.values = values;
+  p.masks = masks;
+  p.X = X;
+  p.ldx = ldx;
+  p.Y = static_cast<__half*>(Y);
+  p.ldy = ldy;
+  p.rows = rows;
+  p.words = (int)(cols / 32);
+  p.T = T;
+  p.wait_limit_ns = (uint64_t)wait_limit_us * 1000u;
+  p.stall_weights = 1;
+  cudaError_t e = launch_spmm_tc(p, 3, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
 int64_t nm_wait_timeouts(int reset) {
   unsigned long long n = 0;
   return read_wait_timeouts(&n, reset) == cudaSuccess ? (int64_t)n : -NM_ERR_CUDA;

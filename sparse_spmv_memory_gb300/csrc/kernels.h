@@ -104,6 +104,8 @@ struct SpmmTcParams {
   int64_t rows;
   int words;                // cols / 32
   int64_t T;                // tokens
+  uint64_t wait_limit_ns = 0;  // bound of every in-kernel wait (0: the default)
+  int stall_weights = 0;       // self-test: the weight producer issues nothing
 };
 
 int spmm_tc_variant_count();

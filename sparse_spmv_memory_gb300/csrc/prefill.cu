@@ -156,7 +156,8 @@ template <int NMMA, int NB, int STAGES, int G, int DG, int DW, bool MT>
 __global__ void __launch_bounds__(threads_for(DW), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
-                   __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy) {
+                   __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy,
+                   uint64_t wait_limit_ns, int stall_weights) {
   using L = Layout<NMMA, NB, STAGES, MT>;
   static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
   static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       int issued = 0;
       for (int kt = 0; kt < words; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
-        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1)) break;
+        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns)) break;
         mbar_arrive_expect_tx(full(s), L::B_BYTES);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
@@ -221,19 +222,22 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       // Teardown must not free shared memory under copies still in flight:
       // wait (bounded) for the last stages issued.
       const int first = issued > STAGES ? issued - STAGES : 0;
-      for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
+      for (int kt = first; kt < issued; ++kt)
+        mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
     }
     __syncwarp();
   } else if (warp == 2) {
     // ---- W producer: compact values (and mask words) of each stage ----------
     // With MT one lane issues TMA; without, all lanes gather the mask words
     // by cp.async, each arriving on the stage barrier when its copies land.
-    if (!MT || lane == 0) {
+    // stall_weights (self-test only) issues nothing: every consumer's bounded
+    // wait then runs out and the block tears down without storing Y.
+    if ((!MT || lane == 0) && !stall_weights) {
       int issued = 0;
       for (int kt = 0; kt < words; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
         int ok = 1;
-        if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1);
+        if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns);
         if (!MT) ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
@@ -261,11 +265,13 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       if (!MT) cp_async_wait_all();
       if (lane == 0) {
         const int first = issued > STAGES ? issued - STAGES : 0;
-        for (int kt = first; kt < issued; ++kt) mbar_wait(full(kt % STAGES), (kt / STAGES) & 1);
+        for (int kt = first; kt < issued; ++kt)
+          mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
         if (MT && issued > 0) {  // the mask boxes still in flight
           const int nbox = (issued + MW - 1) / MW;
           const int b0 = nbox > L::MT_SLOTS ? nbox - L::MT_SLOTS : 0;
-          for (int b = b0; b < nbox; ++b) mbar_wait(mfull(b % L::MT_SLOTS), (b / L::MT_SLOTS) & 1);
+          for (int b = b0; b < nbox; ++b)
+            mbar_wait(mfull(b % L::MT_SLOTS), (b / L::MT_SLOTS) & 1, wait_limit_ns);
         }
       }
     }
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
       for (int kt = 0; kt < words; kt += G) {
         const int last = kt + G - 1 < words ? kt + G - 1 : words - 1;
-        if (!mbar_wait(afull(last % STAGES), (last / STAGES) & 1)) break;
+        if (!mbar_wait(afull(last % STAGES), (last / STAGES) & 1, wait_limit_ns)) break;
         tc_fence_after_sync();
         for (int k = kt; k <= last; ++k) {
           const int s = k % STAGES;
@@ -310,12 +316,12 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     int box = -1;  // mask box this warp last waited for
     for (int kt = grp; kt < words; kt += DG) {
       const int s = kt % STAGES, u = kt / STAGES;
-      bool got = mbar_wait(full(s), u & 1);
+      bool got = mbar_wait(full(s), u & 1, wait_limit_ns);
       if (MT && kt / MW != box) {
         // The box's slot is refilled only after the MMAs of a later stage, so
         // after every group is done with it: its phase here is this box's.
         box = kt / MW;
-        got = got && mbar_wait(mfull(box % L::MT_SLOTS), (box / L::MT_SLOTS) & 1);
+        got = got && mbar_wait(mfull(box % L::MT_SLOTS), (box / L::MT_SLOTS) & 1, wait_limit_ns);
       }
       // The warp decides together, so no lane is left behind at a warp barrier.
       if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(afull(s));
     }
-    if (!mbar_wait(accum, 0)) ok = false;
+    if (!mbar_wait(accum, 0, wait_limit_ns)) ok = false;
     tc_fence_after_sync();
     // tcgen05.ld is a warp-wide instruction: the whole warp reads or none does.
     if (__all_sync(0xFFFFFFFFu, ok)) {
@@ -433,8 +439,9 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(threads_for(DW));
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = stream;
+  const uint64_t limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
   return cudaLaunchKernelEx(&cfg, k, tm_v, tm_x, tm_m, p.masks, p.Y, p.rows, p.words, p.T,
-                            p.ldy);
+                            p.ldy, limit, p.stall_weights);
 }
 
 // Mask words by TMA when the mask array allows it (16-byte aligned, row pitch

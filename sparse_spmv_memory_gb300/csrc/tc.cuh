@@ -59,14 +59,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the barrier's phase with the given parity has completed.
-// Returns false (and counts a timeout) if that takes longer than
-// kWaitLimitNs; the caller then abandons its loop and goes to teardown.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Returns false (and counts a timeout) if that takes longer than limit_ns;
+// the caller then abandons its loop and goes to teardown.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicAdd(&g_wait_timeouts, 1ull);
       return false;
     }

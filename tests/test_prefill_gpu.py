@@ -198,3 +198,30 @@ def test_nm_spmm_beyond_eight_tokens_takes_the_tensor_core_path(nm, orc):
     assert np.array_equal(a, b)
     y_ref, s = oracle_Y(orc, ov, om, cols, X)
     assert np.all(np.abs(f16_to_f64(a) - y_ref) <= oracle.tolerance(s))
+
+
+def test_bounded_waits_end_a_stalled_prefill_kernel(nm, orc):
+    """Self-test of the failure path: with its weight producer disabled no
+    stage ever completes; every wait runs out after the given limit, is
+    counted, the kernel stores nothing and returns, and the device stays
+    usable for the next call (which is exact again)."""
+    import time
+    rows, cols, T = 256, 1024, 64
+    W, X = gen(rows, cols, T, 13)
+    ov, om, v, m = dev_packed(orc, W, 2, 4)
+    Xd = to_dev(X)
+    Y = torch.full((T, rows), 3.0, dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    nm.nm_wait_timeouts(reset=True)
+    t0 = time.time()
+    nm.nm_prefill_stall_selftest(v, m, Xd, Y, wait_limit_us=20000)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert nm.nm_wait_timeouts(reset=True) > 0
+    assert bool((Y == 3.0).all())
+    assert elapsed < 30.0
+    Y2 = f16_to_f64(from_dev(nm.nm_spmm_prefill(v, m, Xd)))
+    torch.cuda.synchronize()
+    y_ref, s = oracle_Y(orc, ov, om, cols, X)
+    assert np.all(np.abs(Y2 - y_ref) <= oracle.tolerance(s))
+    assert nm.nm_wait_timeouts() == 0
