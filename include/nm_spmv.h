@@ -265,7 +265,8 @@ int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *
  * rows == 0 is a no-op.  Y must not overlap any input.  No workspace.
  * nm_spmm_prefill_ex takes a kernel variant (< 0: chosen from T;
  * 0..nm_spmm_prefill_variant_count()-1: 512 tokens per block with 4 pipeline
- * stages, 256, 128, 64 tokens, and 512 tokens with 5 stages).
+ * stages, 256, 128, 64 tokens, and 512 tokens with 5 stages; the default
+ * minimises waves of blocks times each variant's measured time per stage).
  * ------------------------------------------------------------------------- */
 int nm_spmm_prefill(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                     const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, void *stream);

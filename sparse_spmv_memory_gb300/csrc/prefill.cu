@@ -373,8 +373,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
 struct Variant {
   int nmma, nb, stages, g, dg, dw;
 };
-constexpr Variant kVariants[] = {{256, 2, 4, 1, 2, 16}, {256, 1, 6, 1, 2, 16}, {128, 1, 8, 1, 4, 16},
-                                 {64, 1, 8, 1, 4, 16},  {256, 2, 5, 1, 4, 16}};
+// Stage counts are the deepest that fit 227 KB of shared memory (4 for the
+// first 512-token variant, kept as the shallower alternative).
+constexpr Variant kVariants[] = {{256, 2, 4, 1, 2, 16}, {256, 1, 7, 1, 2, 16}, {128, 1, 10, 1, 4, 16},
+                                 {64, 1, 12, 1, 4, 16}, {256, 2, 5, 1, 4, 16}};
 constexpr int kVariantCount = sizeof(kVariants) / sizeof(kVariants[0]);
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -459,14 +461,14 @@ int spmm_tc_variant_count() { return tc::kVariantCount; }
 
 // The variant that minimises (waves of blocks) x (time of one block), with
 // each variant's time per 32-column stage measured on GB300 over the
-// decoder-layer shapes (ns, one block per SM): 512 tokens 453 (5 stages),
-// 256 tokens 352, 128 tokens 288, 64 tokens 279.  A larger token tile does
+// decoder-layer shapes (ns, one block per SM): 512 tokens 452 (5 stages),
+// 256 tokens 308 (7), 128 tokens 254 (10), 64 tokens 247 (12).  A larger token tile does
 // more work per stage, a smaller one fills more SMs when rows are few.
 int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
   static const struct {
     int variant, tokens;
     double ns_per_stage;
-  } cand[] = {{4, 512, 453.0}, {1, 256, 352.0}, {2, 128, 288.0}, {3, 64, 279.0}};
+  } cand[] = {{4, 512, 452.0}, {1, 256, 308.0}, {2, 128, 254.0}, {3, 64, 247.0}};
   if (sms < 1) sms = 1;
   const int64_t row_tiles = (rows + 127) / 128;
   int best = 3;
@@ -489,9 +491,9 @@ int spmm_tc_block_tokens(int variant) {
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
   switch (variant) {
     case 0: return tc::launch_tc<256, 2, 4, 1, 2, 16>(p, stream);
-    case 1: return tc::launch_tc<256, 1, 6, 1, 2, 16>(p, stream);
-    case 2: return tc::launch_tc<128, 1, 8, 1, 4, 16>(p, stream);
-    case 3: return tc::launch_tc<64, 1, 8, 1, 4, 16>(p, stream);
+    case 1: return tc::launch_tc<256, 1, 7, 1, 2, 16>(p, stream);
+    case 2: return tc::launch_tc<128, 1, 10, 1, 4, 16>(p, stream);
+    case 3: return tc::launch_tc<64, 1, 12, 1, 4, 16>(p, stream);
     case 4: return tc::launch_tc<256, 2, 5, 1, 4, 16>(p, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -22,7 +22,7 @@ BM, BK, ROW_BYTES = 128, 32, 64
 A_BYTES, V_BYTES, M_BYTES = BM * ROW_BYTES, BM * 32, BM * 4
 DENSIFY_WARPS = 16
 ROWS_PER_WARP = BM // DENSIFY_WARPS
-VARIANTS = [(256, 2, 4), (256, 1, 6), (128, 1, 8), (64, 1, 8), (256, 2, 5)]
+VARIANTS = [(256, 2, 4), (256, 1, 7), (128, 1, 10), (64, 1, 12), (256, 2, 5)]
 DENSIFY_GROUPS = [2, 2, 4, 4, 4]   # stage-parallel densify groups per variant
 SMEM_OPTIN = 232448  # bytes of dynamic shared memory a GB300 block may opt into
 
