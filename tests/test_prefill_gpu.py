@@ -225,3 +225,32 @@ def test_bounded_waits_end_a_stalled_prefill_kernel(nm, orc):
     y_ref, s = oracle_Y(orc, ov, om, cols, X)
     assert np.all(np.abs(Y2 - y_ref) <= oracle.tolerance(s))
     assert nm.nm_wait_timeouts() == 0
+
+
+def test_prefill_randomised_shapes_bit_exact(nm, orc):
+    """Seeded random shapes (any rows, any multiple of 32 columns, any token
+    count, all four patterns, odd and even word counts so both mask paths
+    run), every variant, exact-arithmetic inputs: bit-exact against the
+    oracle.  Plus the smallest case, one row of 32 columns and one token."""
+    draws = synth.u64(64, 0, synth.stream_id(74))
+    cases = [(1, 32, 1, (2, 4))]
+    for k in range(12):
+        d = [int(x) for x in draws[4 * k: 4 * k + 4]]
+        rows = 1 + d[0] % 700
+        cols = 32 * (1 + d[1] % 100)
+        T = 1 + d[2] % 700
+        if rows * cols * T > 120_000_000:  # keep the oracle to seconds
+            T = max(1, 120_000_000 // (rows * cols))
+        cases.append((rows, cols, T, PATTERNS[d[3] % 4]))
+    for ci, (rows, cols, T, (N, M)) in enumerate(cases):
+        W, X = gen(rows, cols, T, 100 + ci, exact=True)
+        ov, om, v, m = dev_packed(orc, W, N, M)
+        y_ref, _ = oracle_Y(orc, ov, om, cols, X)
+        want = orc.round_f16(y_ref).reshape(y_ref.shape)
+        Xd = to_dev(X)
+        for variant in range(nm.nm_spmm_prefill_variant_count()):
+            got = from_dev(nm.nm_spmm_prefill(v, m, Xd, variant=variant))
+            bad = np.argwhere(got != want)
+            assert bad.size == 0, (f"rows {rows} cols {cols} T {T} {N}:{M} variant {variant}: "
+                                   f"{len(bad)} mismatches, first {bad[:3].tolist()}")
+    assert nm.nm_wait_timeouts() == 0
