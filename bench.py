@@ -651,9 +651,25 @@ def run_gpu(args):
 
     if rank == 0 and world == 1 and args.cpu and args.batch == 1:
         _, nb, dt, desc = oracle_sample(mats, head, args.cpu_seconds)
-        out["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+        out["cpu_baseline"] = {**host_cpu(), "value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
     return out
+
+
+def host_cpu():
+    """The host the oracle runs on: logical CPUs and a model string."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return {"host_logical_cpus": os.cpu_count(), "host_cpu": model or os.uname().machine}
 
 
 def prefill_flops(mats, T):
@@ -810,7 +826,7 @@ def run_prefill(args):
     }
     if rank == 0 and world == 1 and args.cpu:
         rate, desc, dt = oracle_prefill_rate(mats, head, args.cpu_seconds)
-        out["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": 1,
+        out["cpu_baseline"] = {**host_cpu(), "value": round(rate, 6), "unit": "TFLOP/s", "cores": 1,
                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
     return out
 
@@ -832,7 +848,8 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
             "config": {"workload": f"{args.workload}, prefill {args.prefill} tokens, oracle sample",
                        "pattern": args.pattern},
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(rate, 6),
+            "cpu_baseline": {**host_cpu(), "kind": "oracle", "cores": 1, "sample": desc,
+                             "value": round(rate, 6),
                              "unit": "TFLOP/s"},
             "e2e": {"value": round(rate, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -854,7 +871,8 @@ def run_reference(args):
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
         "config": {"workload": f"{args.workload}, batch 1, oracle sample", "pattern": args.pattern},
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(val, 4),
+        "cpu_baseline": {**host_cpu(), "kind": "oracle", "cores": 1, "sample": desc,
+                         "value": round(val, 4),
                          "unit": "GB/s"},
         "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
