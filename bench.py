@@ -799,7 +799,9 @@ def run_prefill(args):
                          + ", ".join(f"{n} {r}x{c}" for n, r, c in mats)),
             "pattern": f"{head[0]}:{head[1]}", "calls_per_step": layers * len(mats),
             "physical_slots": 2,
-            "l2_defeat": "not needed: compute-bound (each call re-reads its tiles from L2 by design)",
+            "l2_defeat": (f"inputs larger than L2: 2 packed layer slots of "
+                          f"{sum(sparse_bytes(r, c) for _, r, c in mats) / 1e9:.2f} GB each "
+                          "(129 MB L2) cycled over the layers"),
             "parallelism": f"replicas x{world}", "kernel_variant": "library default for T",
         },
         "gpu_launches": layers * len(mats) * k,
