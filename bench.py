@@ -657,18 +657,21 @@ def run_gpu(args):
 
 
 def host_cpu():
-    """The host the oracle runs on: logical CPUs and a model string."""
-    model = ""
+    """The host the oracle runs on: logical CPUs and a model string (the
+    model name on x86; architecture, implementer and part codes on Arm)."""
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu part", "hardware") and ":" in line:
-                    model = line.split(":", 1)[1].strip()
-                    if key == "model name":
-                        break
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
     except OSError:
         pass
+    model = fields.get("model name")
+    if not model and "cpu part" in fields:
+        model = (f"{os.uname().machine} (implementer {fields.get('cpu implementer', '?')}, "
+                 f"part {fields['cpu part']})")
     return {"host_logical_cpus": os.cpu_count(), "host_cpu": model or os.uname().machine}
 
 
