@@ -57,8 +57,12 @@ constexpr int MT_SLOT = BM * MW * 4;   // 2 KiB: the masks of MW consecutive sta
 // Densify warps per block (DW, a kernel parameter) follow the producer and
 // MMA warps.  16 measured best on GB300: 8 left the per-stage chains
 // exposed, 24 lost to the extra shared-memory and issue contention.
+// After them: a second MMA issuer (used by the K-split variants) and the
+// producer of the mask boxes.
 constexpr int FIRST_DENSIFY_WARP = 3;
-__host__ __device__ constexpr int threads_for(int dw) { return (FIRST_DENSIFY_WARP + dw) * 32; }
+__host__ __device__ constexpr int mma2_warp(int dw) { return FIRST_DENSIFY_WARP + dw; }
+__host__ __device__ constexpr int mask_warp(int dw) { return FIRST_DENSIFY_WARP + dw + 1; }
+__host__ __device__ constexpr int threads_for(int dw) { return (FIRST_DENSIFY_WARP + dw + 2) * 32; }
 
 constexpr uint32_t tmem_cols_for(int n) {
   return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
@@ -71,7 +75,9 @@ constexpr uint32_t tmem_cols_for(int n) {
 // after the MMA (hence the densify) of stage kt + MW * MT_SLOTS - STAGES is
 // done, which is at or after the slot's last reader kt + MW - 1 when
 // MW * MT_SLOTS >= STAGES + MW - 1.
-template <int NMMA, int NB, int STAGES, bool MT>
+// MS: 0, one thread issues every stage's MMAs; 1, two threads take the even
+// and odd stages into two accumulators that the epilogue adds (K split).
+template <int NMMA, int NB, int STAGES, int MS, bool MT>
 struct Layout {
   static constexpr int BN = NMMA * NB;
   static constexpr int B_BYTES = BN * ROW_BYTES;
@@ -86,7 +92,8 @@ struct Layout {
   static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1 + MT_SLOTS) * 8;
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
-  static constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
+  static constexpr uint32_t TMEM_COLS = tmem_cols_for(MS ? 2 * BN : BN);
+  static_assert(!MS || 2 * BN <= 512, "the K split keeps two accumulators in tensor memory");
   static_assert(!MT || MW * MT_SLOTS >= STAGES + MW - 1, "mask slot reused too early");
   static_assert(NMMA % 16 == 0 && NMMA >= 16 && NMMA <= 256, "tcgen05 M=128 needs N in 16..256");
   static_assert(BN >= 64 && BN <= 512 && BN % 32 == 0, "epilogue reads 32-column chunks");
@@ -152,14 +159,15 @@ __device__ __forceinline__ void densify_stage(uint32_t sA, uint32_t sV, uint32_t
 // ... with 128 / (16 / DG) rows per warp.  Each stage costs a warp a fixed
 // chain of barrier waits, fences and arrivals (hundreds of cycles of
 // latency) besides its rows, so with DG groups that chain overlaps DG stages.
-template <int NMMA, int NB, int STAGES, int G, int DG, int DW, bool MT>
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW, int MS, bool MT>
 __global__ void __launch_bounds__(threads_for(DW), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
                    __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy,
                    uint64_t wait_limit_ns, int stall_weights) {
-  using L = Layout<NMMA, NB, STAGES, MT>;
+  using L = Layout<NMMA, NB, STAGES, MS, MT>;
   static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
+  static_assert(MS == 0 || G == 1, "each K-split issuer waits on each of its stages");
   static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
   static_assert(threads_for(DW) <= 1024, "a block has at most 1024 threads");
   static_assert(DG <= MW, "every densify group must read every mask box, in order");
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       mbar_init(empty(s), 1);                 // tcgen05.commit
       mbar_init(afull(s), WPG);               // one arrival per warp of the stage's group
     }
-    mbar_init(accum, 1);
+    mbar_init(accum, MS ? 2 : 1);             // final commit of each issuer
     for (int m = 0; m < L::MT_SLOTS; ++m) mbar_init(mfull(m), 1);
     fence_mbar_init();
     prefetch_tmap(&tm_v);
@@ -227,9 +235,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ---- W producer: compact values (and mask words) of each stage ----------
-    // With MT one lane issues TMA; without, all lanes gather the mask words
-    // by cp.async, each arriving on the stage barrier when its copies land.
+    // ---- W producer: compact values (and, without MT, mask words) ----------
+    // With MT one lane issues the values' TMA (the mask boxes have a warp of
+    // their own); without, all lanes also gather the mask words by cp.async,
+    // each arriving on the stage barrier when its copies land.
     // stall_weights (self-test only) issues nothing: every consumer's bounded
     // wait then runs out and the block tears down without storing Y.
     if ((!MT || lane == 0) && !stall_weights) {
@@ -241,11 +250,6 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
         if (!MT) ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          if (MT && kt % MW == 0) {
-            const int ms = (kt / MW) % L::MT_SLOTS;
-            mbar_arrive_expect_tx(mfull(ms), MT_SLOT);
-            tma_load_2d(sM + ms * MT_SLOT, &tm_m, kt, (int)r0, mfull(ms));
-          }
           mbar_arrive_expect_tx(full(s), V_BYTES);
           tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
         }
@@ -267,27 +271,45 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
         const int first = issued > STAGES ? issued - STAGES : 0;
         for (int kt = first; kt < issued; ++kt)
           mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
-        if (MT && issued > 0) {  // the mask boxes still in flight
-          const int nbox = (issued + MW - 1) / MW;
-          const int b0 = nbox > L::MT_SLOTS ? nbox - L::MT_SLOTS : 0;
-          for (int b = b0; b < nbox; ++b)
-            mbar_wait(mfull(b % L::MT_SLOTS), (b / L::MT_SLOTS) & 1, wait_limit_ns);
-        }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---- MMA issuer ----------------------------------------------------
-    // Waits only on the densify barriers: the densify warps saw the stage's
-    // "full" barrier complete (so the TMA-loaded X tile is visible through
-    // their release-arrive).  With one densify group (DG == 1) every warp
-    // arrives on the stages in order, so G = 2 may wait on every second
-    // barrier only (afull(kt + 1) complete implies afull(kt)); with several
-    // groups each stage's barrier is waited on (G = 1).
-    if (lane == 0) {
+  } else if (warp == mask_warp(DW)) {
+    // ---- mask producer (MT): one box of MW stages' mask words at a time -----
+    // A box's slot is refilled at stage kt only after the MMAs of stage
+    // kt - STAGES, hence every densify of the slot's previous box, are done.
+    if (MT && lane == 0 && !stall_weights) {
+      int nbox = 0;
+      for (int kt = 0; kt < words; kt += MW) {
+        const int s = kt % STAGES, u = kt / STAGES;
+        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns)) break;
+        const int ms = (kt / MW) % L::MT_SLOTS;
+        mbar_arrive_expect_tx(mfull(ms), MT_SLOT);
+        tma_load_2d(sM + ms * MT_SLOT, &tm_m, kt, (int)r0, mfull(ms));
+        nbox = kt / MW + 1;
+      }
+      const int b0 = nbox > L::MT_SLOTS ? nbox - L::MT_SLOTS : 0;  // boxes still in flight
+      for (int b = b0; b < nbox; ++b)
+        mbar_wait(mfull(b % L::MT_SLOTS), (b / L::MT_SLOTS) & 1, wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == mma2_warp(DW)) {
+    // ---- MMA issuers ----------------------------------------------------
+    // Each waits only on the densify barriers: the densify warps saw the
+    // stage's "full" barrier complete (so the TMA-loaded X tile is visible
+    // through their release-arrive).  With one densify group (DG == 1) every
+    // warp arrives on the stages in order, so G = 2 may wait on every second
+    // barrier only (afull(kt + 1) complete implies afull(kt)).  A barrier test,
+    // a commit and each tcgen05.mma cost the issuing thread tens to hundreds
+    // of cycles, so with MS == 1 two threads share the stages (even / odd,
+    // into two accumulators).
+    const int role = warp == 1 ? 0 : 1;
+    if (lane == 0 && (role == 0 || MS != 0)) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
-      for (int kt = 0; kt < words; kt += G) {
-        const int last = kt + G - 1 < words ? kt + G - 1 : words - 1;
+      const int k0 = MS ? role : 0, kstep = MS ? 2 : G;
+      const uint32_t dacc = tmem_base + (uint32_t)(MS && role ? L::BN : 0);
+      for (int kt = k0; kt < words; kt += kstep) {
+        const int last = MS ? kt : (kt + G - 1 < words ? kt + G - 1 : words - 1);
         if (!mbar_wait(afull(last % STAGES), (last / STAGES) & 1, wait_limit_ns)) break;
         tc_fence_after_sync();
         for (int k = kt; k <= last; ++k) {
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
             for (int j = 0; j < NB; ++j) {
               const uint64_t bd =
                   smem_desc_sw64(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES + ks * 32);
-              mma_f16(tmem_base + (uint32_t)(j * NMMA), ad, bd, idesc, (k | ks) != 0);
+              mma_f16(dacc + (uint32_t)(j * NMMA), ad, bd, idesc, (k != k0) || (ks != 0));
             }
           }
           mma_commit(empty(s));
@@ -350,6 +372,14 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
         uint32_t v[32];
         tmem_ld_32(tbase + (uint32_t)c0, v);
         tmem_ld_wait();
+        if (MS && words > 1) {  // the odd stages' accumulator (none when words == 1)
+          uint32_t w[32];
+          tmem_ld_32(tbase + (uint32_t)(L::BN + c0), w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
+        }
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -371,12 +401,13 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
 
 // ---- host ------------------------------------------------------------------
 struct Variant {
-  int nmma, nb, stages, g, dg, dw;
+  int nmma, nb, stages, g, dg, dw, ms;
 };
 // Stage counts are the deepest that fit 227 KB of shared memory (4 for the
 // first 512-token variant, kept as the shallower alternative).
-constexpr Variant kVariants[] = {{256, 2, 4, 1, 2, 16}, {256, 1, 7, 1, 2, 16}, {128, 1, 10, 1, 4, 16},
-                                 {64, 1, 12, 1, 4, 16}, {256, 2, 5, 1, 4, 16}};
+constexpr Variant kVariants[] = {{256, 2, 4, 1, 2, 16, 0},  {256, 1, 7, 1, 2, 16, 1},
+                                 {128, 1, 10, 1, 4, 16, 1}, {64, 1, 12, 1, 4, 16, 1},
+                                 {256, 2, 5, 1, 4, 16, 0}};
 constexpr int kVariantCount = sizeof(kVariants) / sizeof(kVariants[0]);
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -412,9 +443,9 @@ static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMMA, int NB, int STAGES, int G, int DG, int DW, bool MT>
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW, int MS, bool MT>
 static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
-  using L = Layout<NMMA, NB, STAGES, MT>;
+  using L = Layout<NMMA, NB, STAGES, MS, MT>;
   CUtensorMap tm_v, tm_x, tm_m;
   memset(&tm_m, 0, sizeof(tm_m));
   if (MT && !encode_2d(&tm_m, p.masks, (uint64_t)p.words, (uint64_t)p.rows,
@@ -426,7 +457,7 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
       !encode_2d(&tm_x, p.X, (uint64_t)p.words * 32, (uint64_t)p.T, (uint64_t)p.ldx * 2, BK,
                  NMMA, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, G, DG, DW, MT>;
+  auto* k = spmm_tc_kernel<NMMA, NB, STAGES, G, DG, DW, MS, MT>;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -448,11 +479,11 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
 
 // Mask words by TMA when the mask array allows it (16-byte aligned, row pitch
 // words * 4 a multiple of 16: every decoder shape), else by cp.async.
-template <int NMMA, int NB, int STAGES, int G, int DG, int DW>
+template <int NMMA, int NB, int STAGES, int G, int DG, int DW, int MS>
 static cudaError_t launch_tc(const SpmmTcParams& p, cudaStream_t stream) {
   const bool mt = p.words % 4 == 0 && (reinterpret_cast<uintptr_t>(p.masks) & 15) == 0;
-  return mt ? launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, true>(p, stream)
-            : launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, false>(p, stream);
+  return mt ? launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, MS, true>(p, stream)
+            : launch_tc_mt<NMMA, NB, STAGES, G, DG, DW, MS, false>(p, stream);
 }
 
 }  // namespace tc
@@ -461,14 +492,14 @@ int spmm_tc_variant_count() { return tc::kVariantCount; }
 
 // The variant that minimises (waves of blocks) x (time of one block), with
 // each variant's time per 32-column stage measured on GB300 over the
-// decoder-layer shapes (ns, one block per SM): 512 tokens 452 (5 stages),
-// 256 tokens 308 (7), 128 tokens 254 (10), 64 tokens 247 (12).  A larger token tile does
+// decoder-layer shapes (ns, one block per SM): 512 tokens 444 (5 stages),
+// 256 tokens 309 (7), 128 tokens 223 (10), 64 tokens 210 (12).  A larger token tile does
 // more work per stage, a smaller one fills more SMs when rows are few.
 int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
   static const struct {
     int variant, tokens;
     double ns_per_stage;
-  } cand[] = {{4, 512, 452.0}, {1, 256, 308.0}, {2, 128, 254.0}, {3, 64, 247.0}};
+  } cand[] = {{4, 512, 444.0}, {1, 256, 309.0}, {2, 128, 223.0}, {3, 64, 210.0}};
   if (sms < 1) sms = 1;
   const int64_t row_tiles = (rows + 127) / 128;
   int best = 3;
@@ -490,11 +521,11 @@ int spmm_tc_block_tokens(int variant) {
 
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
   switch (variant) {
-    case 0: return tc::launch_tc<256, 2, 4, 1, 2, 16>(p, stream);
-    case 1: return tc::launch_tc<256, 1, 7, 1, 2, 16>(p, stream);
-    case 2: return tc::launch_tc<128, 1, 10, 1, 4, 16>(p, stream);
-    case 3: return tc::launch_tc<64, 1, 12, 1, 4, 16>(p, stream);
-    case 4: return tc::launch_tc<256, 2, 5, 1, 4, 16>(p, stream);
+    case 0: return tc::launch_tc<256, 2, 4, 1, 2, 16, 0>(p, stream);
+    case 1: return tc::launch_tc<256, 1, 7, 1, 2, 16, 1>(p, stream);
+    case 2: return tc::launch_tc<128, 1, 10, 1, 4, 16, 1>(p, stream);
+    case 3: return tc::launch_tc<64, 1, 12, 1, 4, 16, 1>(p, stream);
+    case 4: return tc::launch_tc<256, 2, 5, 1, 4, 16, 0>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -24,6 +24,7 @@ DENSIFY_WARPS = 16
 ROWS_PER_WARP = BM // DENSIFY_WARPS
 VARIANTS = [(256, 2, 4), (256, 1, 7), (128, 1, 10), (64, 1, 12), (256, 2, 5)]
 DENSIFY_GROUPS = [2, 2, 4, 4, 4]   # stage-parallel densify groups per variant
+MMA_SPLIT = [0, 1, 1, 1, 0]        # 1: two issuers, even / odd stages into two accumulators
 SMEM_OPTIN = 232448  # bytes of dynamic shared memory a GB300 block may opt into
 
 
@@ -211,10 +212,11 @@ def test_layout_fits_and_is_aligned(nmma, nb, stages, mt):
     assert 2 * L["SMEM"] > SMEM_OPTIN + 1024      # one block per SM: TMEM never contended
     assert L["B_OFF"] % 1024 == 0 and (nmma * ROW_BYTES) % 1024 == 0
     assert L["BAR_OFF"] % 8 == 0
+    acc_cols = L["BN"] * (2 if MMA_SPLIT[VARIANTS.index((nmma, nb, stages))] else 1)
     tmem = 32
-    while tmem < L["BN"]:
+    while tmem < acc_cols:
         tmem *= 2
-    assert tmem <= 512 and L["BN"] <= tmem
+    assert tmem <= 512 and acc_cols <= tmem
     # epilogue: the quadrant's warps stride the BN columns in 32-column loads
     assert L["BN"] % 32 == 0
 
