@@ -71,10 +71,9 @@ constexpr uint32_t tmem_cols_for(int n) {
 // MT: masks arrive by TMA, MW stages' worth per box, into MT_SLOTS slots
 // (needs the row pitch of the mask array, words * 4 bytes, to be a multiple
 // of 16); otherwise by 4-byte cp.async into a per-stage ring.  A slot is
-// refilled at stage kt + MW * MT_SLOTS; the producer issues that stage only
-// after the MMA (hence the densify) of stage kt + MW * MT_SLOTS - STAGES is
-// done, which is at or after the slot's last reader kt + MW - 1 when
-// MW * MT_SLOTS >= STAGES + MW - 1.
+// refilled once every densify warp has released it (a barrier per slot);
+// MW * MT_SLOTS >= STAGES + MW - 1 boxes in flight keep the box of every
+// stage in the pipeline resident while the densify warps reach it.
 // MS: 0, one thread issues every stage's MMAs; 1, two threads take the even
 // and odd stages into two accumulators that the epilogue adds (K split).
 template <int NMMA, int NB, int STAGES, int MS, bool MT>
@@ -87,9 +86,9 @@ struct Layout {
   static constexpr int M_OFF = V_OFF + STAGES * V_BYTES;
   static constexpr int MT_SLOTS = (STAGES + MW - 1 + MW - 1) / MW;
   static constexpr int M_REGION = MT ? MT_SLOTS * MT_SLOT : STAGES * M_BYTES;
-  // barriers: full, empty, afull (per stage), accum, mfull (per mask slot)
+  // barriers: full, empty, afull (per stage), accum, mfull, mfree (per mask slot)
   static constexpr int BAR_OFF = M_OFF + M_REGION;
-  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1 + MT_SLOTS) * 8;
+  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1 + 2 * MT_SLOTS) * 8;
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(MS ? 2 * BN : BN);
@@ -185,6 +184,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   // A mask box serves MW consecutive stages that may belong to different
   // densify groups, so it completes on a barrier of its own.
   auto mfull = [&](int slot) { return bars + 8u * (3 * STAGES + 1 + slot); };
+  // ... and is released on one when every densify warp has finished its last
+  // stage in the box (the stages of a box may go to different MMA issuers, so
+  // no single stage's completion implies that).
+  auto mfree = [&](int slot) { return bars + 8u * (3 * STAGES + 1 + L::MT_SLOTS + slot); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = (int64_t)blockIdx.y * BM;
@@ -197,7 +200,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       mbar_init(afull(s), WPG);               // one arrival per warp of the stage's group
     }
     mbar_init(accum, MS ? 2 : 1);             // final commit of each issuer
-    for (int m = 0; m < L::MT_SLOTS; ++m) mbar_init(mfull(m), 1);
+    for (int m = 0; m < L::MT_SLOTS; ++m) {
+      mbar_init(mfull(m), 1);
+      mbar_init(mfree(m), DW);
+    }
     fence_mbar_init();
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_x);
@@ -213,10 +219,20 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   uint32_t tmem_base;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem_base) : "r"(slot) : "memory");
 
+  // Teardown must not free shared memory under copies still in flight: a
+  // producer waits (bounded) for the stages it issued among the last STAGES
+  // of the row -- the final use of each slot, so the phase it waits for is
+  // the slot's last.  A producer that stopped early on a timeout issued
+  // nothing in the last 2 s worth waiting for.
+  auto drain = [&](int last) {
+    for (int kt = last; kt >= 0 && kt > words - 1 - STAGES; --kt)
+      mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
+  };
+
   if (warp == 0) {
-    // ---- X producer: the token tile of each stage -----------------------
+    // ---- X producer: the token tile of each stage -------------------------
     if (lane == 0) {
-      int issued = 0;
+      int last = -1;
       for (int kt = 0; kt < words; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
         if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns)) break;
@@ -225,13 +241,9 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
         for (int j = 0; j < NB; ++j)
           tma_load_2d(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES, &tm_x, kt * BK,
                       (int)(n0 + j * NMMA), full(s));
-        issued = kt + 1;
+        last = kt;
       }
-      // Teardown must not free shared memory under copies still in flight:
-      // wait (bounded) for the last stages issued.
-      const int first = issued > STAGES ? issued - STAGES : 0;
-      for (int kt = first; kt < issued; ++kt)
-        mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
+      drain(last);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     // stall_weights (self-test only) issues nothing: every consumer's bounded
     // wait then runs out and the block tears down without storing Y.
     if ((!MT || lane == 0) && !stall_weights) {
-      int issued = 0;
+      int last = -1;
       for (int kt = 0; kt < words; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
         int ok = 1;
@@ -264,26 +276,24 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
           }
           cp_async_arrive_noinc(full(s));
         }
-        issued = kt + 1;
+        last = kt;
       }
       if (!MT) cp_async_wait_all();
-      if (lane == 0) {
-        const int first = issued > STAGES ? issued - STAGES : 0;
-        for (int kt = first; kt < issued; ++kt)
-          mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
-      }
+      if (lane == 0) drain(last);
     }
     __syncwarp();
   } else if (warp == mask_warp(DW)) {
     // ---- mask producer (MT): one box of MW stages' mask words at a time -----
-    // A box's slot is refilled at stage kt only after the MMAs of stage
-    // kt - STAGES, hence every densify of the slot's previous box, are done.
+    // A slot is refilled only after every densify warp released it from the
+    // slot's previous box.  This warp alone refills, in box order, so the
+    // release waited for is always the previous box's.
     if (MT && lane == 0 && !stall_weights) {
       int nbox = 0;
       for (int kt = 0; kt < words; kt += MW) {
-        const int s = kt % STAGES, u = kt / STAGES;
-        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns)) break;
-        const int ms = (kt / MW) % L::MT_SLOTS;
+        const int b = kt / MW, ms = b % L::MT_SLOTS;
+        if (b >= L::MT_SLOTS &&
+            !mbar_wait(mfree(ms), ((b / L::MT_SLOTS) - 1) & 1, wait_limit_ns))
+          break;
         mbar_arrive_expect_tx(mfull(ms), MT_SLOT);
         tma_load_2d(sM + ms * MT_SLOT, &tm_m, kt, (int)r0, mfull(ms));
         nbox = kt / MW + 1;
@@ -340,8 +350,8 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       const int s = kt % STAGES, u = kt / STAGES;
       bool got = mbar_wait(full(s), u & 1, wait_limit_ns);
       if (MT && kt / MW != box) {
-        // The box's slot is refilled only after the MMAs of a later stage, so
-        // after every group is done with it: its phase here is this box's.
+        // The box's slot is refilled only after every densify warp released
+        // it, so the phase this warp sees here is this box's.
         box = kt / MW;
         got = got && mbar_wait(mfull(box % L::MT_SLOTS), (box / L::MT_SLOTS) & 1, wait_limit_ns);
       }
@@ -355,7 +365,12 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       // (one arrival per warp: 32 arrivals on one barrier word serialise).
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(afull(s));
+      if (lane == 0) {
+        mbar_arrive(afull(s));
+        // This warp's last stage in the mask box: it has read the box (its
+        // loads precede the release-arrive), so the slot may be refilled.
+        if (MT && kt + DG >= MW * (kt / MW + 1)) mbar_arrive(mfree((kt / MW) % L::MT_SLOTS));
+      }
     }
     if (!mbar_wait(accum, 0, wait_limit_ns)) ok = false;
     tc_fence_after_sync();
@@ -492,14 +507,14 @@ int spmm_tc_variant_count() { return tc::kVariantCount; }
 
 // The variant that minimises (waves of blocks) x (time of one block), with
 // each variant's time per 32-column stage measured on GB300 over the
-// decoder-layer shapes (ns, one block per SM): 512 tokens 444 (5 stages),
-// 256 tokens 309 (7), 128 tokens 223 (10), 64 tokens 210 (12).  A larger token tile does
+// decoder-layer shapes (ns, one block per SM): 512 tokens 441 (5 stages),
+// 256 tokens 319 (7), 128 tokens 232 (10), 64 tokens 218 (12).  A larger token tile does
 // more work per stage, a smaller one fills more SMs when rows are few.
 int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
   static const struct {
     int variant, tokens;
     double ns_per_stage;
-  } cand[] = {{4, 512, 444.0}, {1, 256, 309.0}, {2, 128, 223.0}, {3, 64, 210.0}};
+  } cand[] = {{4, 512, 441.0}, {1, 256, 319.0}, {2, 128, 232.0}, {3, 64, 218.0}};
   if (sms < 1) sms = 1;
   const int64_t row_tiles = (rows + 127) / 128;
   int best = 3;

@@ -190,18 +190,82 @@ def test_densify_groups_split_stages_and_read_every_mask_box():
         assert sorted(seen) == list(range(words))
 
 
-def test_mask_slots_are_not_refilled_before_their_last_reader():
-    """With masks loaded by TMA (MW stages per box into mt_slots slots) the
-    producer refills a slot at stage kt + MW * slots only after the stage
-    STAGES earlier has been multiplied, i.e. after every densify of the
-    slot's previous MW stages."""
-    for _, _, stages in VARIANTS:
-        n = mt_slots(stages)
-        for kt in range(0, 64, MW):                # a group's first stage
-            refill = kt + MW * n                   # stage that reloads the same slot
-            done_before_refill = refill - stages   # MMA (so densify) finished for <= this
-            assert done_before_refill >= kt + MW - 1
-        assert MW * (n - 1) < stages + MW - 1      # and no slot more than needed
+def _run_pipeline(stages, dg, split, words, rng, warps_per_group=2):
+    """Event model of one block's barrier protocol with masks by TMA: the X/W
+    producer (stage kt once the MMAs of stage kt - STAGES are done), the mask
+    producer (box b once every densify warp released box b - slots), densify
+    warps (group g takes stages g, g + DG, ...; each needs the stage's tiles
+    and its mask box in its slot, and releases the box after its last stage
+    there) and one or two MMA issuers (with the K split: even / odd stages).
+    Actors move in random order.  Asserts that no slot is refilled while a
+    warp still has to read the box it holds, and that the block never
+    deadlocks."""
+    slots = mt_slots(stages)
+    nbox = words // MW
+    nwarps = dg * warps_per_group
+    full, mma_done = [False] * words, [False] * words
+    afull, released = [0] * words, [0] * nbox
+    slot_box = [-1] * slots
+    xw_next, mask_next = 0, 0
+    warp_next = [w // warps_per_group for w in range(nwarps)]
+    issuers = 2 if split else 1
+    mma_next = list(range(issuers))
+
+    def still_needs(w, b):
+        return any(k // MW == b for k in range(warp_next[w], words, dg))
+
+    while not all(mma_done):
+        moves = []
+        if xw_next < words and (xw_next < stages or mma_done[xw_next - stages]):
+            moves.append(("xw",))
+        if mask_next < nbox and (mask_next < slots or released[mask_next - slots] == nwarps):
+            moves.append(("mask",))
+        for w in range(nwarps):
+            kt = warp_next[w]
+            if kt < words and full[kt] and slot_box[(kt // MW) % slots] == kt // MW:
+                moves.append(("dens", w))
+        for i in range(issuers):
+            kt = mma_next[i]
+            if kt < words and afull[kt] == warps_per_group:
+                moves.append(("mma", i))
+        assert moves, "deadlock"
+        m = moves[rng.integers(len(moves))]
+        if m[0] == "xw":
+            full[xw_next] = True
+            xw_next += 1
+        elif m[0] == "mask":
+            s = mask_next % slots
+            if slot_box[s] >= 0:
+                assert not any(still_needs(w, slot_box[s]) for w in range(nwarps))
+            slot_box[s] = mask_next
+            mask_next += 1
+        elif m[0] == "dens":
+            w = m[1]
+            kt = warp_next[w]
+            afull[kt] += 1
+            if kt + dg >= MW * (kt // MW + 1):   # this warp's last stage in the box
+                released[kt // MW] += 1
+            warp_next[w] += dg
+        else:
+            i = m[1]
+            mma_done[mma_next[i]] = True
+            mma_next[i] += issuers if split else 1
+    assert released == [nwarps] * nbox
+
+
+@pytest.mark.parametrize("vi", range(len(VARIANTS)))
+def test_mask_slots_are_not_refilled_before_their_last_reader(vi):
+    """Every densify group touches every box (DG <= MW) and releases it once
+    per warp; the mask producer's wait on the release barrier then keeps each
+    slot until its last reader is done, whatever the order the two K-split
+    issuers and the groups run in, and the pipeline always completes."""
+    _, _, stages = VARIANTS[vi]
+    dg, split = DENSIFY_GROUPS[vi], MMA_SPLIT[vi]
+    assert dg <= MW
+    rng = np.random.default_rng(1234 + vi)
+    for words in (MW, 2 * MW, 4 * MW, 64, 256):
+        for _ in range(6):
+            _run_pipeline(stages, dg, split, words, rng)
 
 
 @pytest.mark.parametrize("mt", [True, False])
@@ -238,3 +302,14 @@ def test_instruction_and_smem_descriptors():
     s = sdesc(0x2C400 + 32)
     assert s & 0x3FFF == (0x2C400 + 32) >> 4
     assert (s >> 32) & 0x3FFF == 32 and (s >> 46) & 3 == 1 and s >> 61 == 4
+
+
+def test_teardown_drain_waits_only_on_final_uses_of_a_slot():
+    """A producer's teardown waits on the stage barriers of the last STAGES
+    stages of the row.  Each is the final use of its slot, so the barrier's
+    last completed phase is the one waited for (a slot reused later would
+    make the parity wait see a later phase and run out)."""
+    for _, _, stages in VARIANTS:
+        for words in range(1, 80):
+            for kt in range(words - 1, max(-1, words - 1 - stages), -1):
+                assert not [k for k in range(kt + 1, words) if k % stages == kt % stages]
