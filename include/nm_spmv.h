@@ -164,13 +164,14 @@ int nm_spmv_swiglu_ex(const void *values, const uint32_t *masks, int64_t rows, i
  *   workspace : device scratch, 16-byte aligned, of at least
  *       nm_spmm_workspace_bytes(rows, cols, batch) bytes (0 when a whole row's
  *       x tile fits in one block's shared memory, else fp32 partial sums of
- *       column slices).  May be NULL when that is 0.
+ *       column slices; for batch > 8, nm_spmm_prefill_workspace_bytes).  May
+ *       be NULL when that is 0.
  * Same arithmetic, rounding, determinism and structural-zero rule as nm_spmv
  * (a non-finite activation of token j reaches only column j of Y); each column of Y is
  * within the same tolerance of the exact product (and equals nm_spmv's
  * result whenever the sums are exact).  nm_spmm with batch > 8 is served by
- * nm_spmm_prefill (tensor cores; workspace ignored; its numerics); nm_spmm_ex
- * and the workspace queries take batch 1..8 only.  batch < 1 -> NM_ERR_SHAPE;
+ * nm_spmm_prefill_ws (tensor cores; its numerics); nm_spmm_ex and
+ * nm_spmm_workspace_bytes_ex take batch 1..8 only.  batch < 1 -> NM_ERR_SHAPE;
  * a short workspace -> NM_ERR_WORKSPACE.  Y must not overlap any input or the
  * workspace.
  * ------------------------------------------------------------------------- */
@@ -262,17 +263,41 @@ int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *
  * tensor core's summation order is fixed, so repeated calls give identical
  * bits; each element is within the nm_spmv tolerance of the exact product.
  * Limits: rows < 2^31 and ceil(rows / 128) <= 65535; T < 2^31.  T == 0 or
- * rows == 0 is a no-op.  Y must not overlap any input.  No workspace.
- * nm_spmm_prefill_ex takes a kernel variant (< 0: chosen from T;
+ * rows == 0 is a no-op.  Y must not overlap any input.  No workspace: every
+ * block multiplies whole rows of W.
+ *
+ * nm_spmm_prefill_ws -- the same product with a K split when it is faster:
+ * when a matrix has too few 128-row tiles to fill the SMs (few rows, or few
+ * tokens), the mask words of each row are cut into S slices (multiples of
+ * four words) taken by different blocks.  Each writes its slice's fp32 sums
+ * to the workspace ([S][T][rows] fp32), and a second kernel adds the S sums
+ * in slice order and rounds once to fp16: deterministic, within the same
+ * tolerance (fp32 sums of fp16 products, one rounding).
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *       nm_spmm_prefill_workspace_bytes(rows, cols, T) bytes (0 when the plan
+ *       for this shape on this device does not split); may be NULL then.  A
+ *       short workspace -> NM_ERR_WORKSPACE; it must not overlap any argument.
+ * nm_spmm_prefill_ex takes the plan explicitly: variant (< 0: chosen;
  * 0..nm_spmm_prefill_variant_count()-1: 512 tokens per block with 4 pipeline
- * stages, 256, 128, 64 tokens, and 512 tokens with 5 stages; the default
- * minimises waves of blocks times each variant's measured time per stage).
+ * stages, 256, 128, 64 tokens, and 512 tokens with 5 stages) and splits
+ * (<= 0: chosen; 1: none; k <= 64: at most k slices -- the words are cut in
+ * multiples of four, so fewer may result); the workspace it needs is
+ * nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, variant, splits).  The
+ * chosen plan minimises a time model: waves of blocks x (a slice's stages x
+ * each variant's measured time per stage + a block's fixed cost), plus the
+ * combine's launch and traffic when split.
  * ------------------------------------------------------------------------- */
 int nm_spmm_prefill(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                     const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, void *stream);
+size_t nm_spmm_prefill_workspace_bytes(int64_t rows, int64_t cols, int64_t T);
+int nm_spmm_prefill_ws(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                       const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy,
+                       void *workspace, size_t workspace_bytes, void *stream);
+size_t nm_spmm_prefill_workspace_bytes_ex(int64_t rows, int64_t cols, int64_t T, int variant,
+                                          int splits);
 int nm_spmm_prefill_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                        const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, int variant,
-                       void *stream);
+                       int splits, void *workspace, size_t workspace_bytes, void *stream);
 int nm_spmm_prefill_variant_count(void);
 
 /* nm_wait_timeouts -- how many times a tensor-core kernel's bounded wait on

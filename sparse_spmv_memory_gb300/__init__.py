@@ -27,7 +27,8 @@ __all__ = [
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
     "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
-    "nm_spmv_swiglu", "nm_spmm_prefill", "nm_spmm_prefill_variant_count", "nm_wait_timeouts",
+    "nm_spmv_swiglu", "nm_spmm_prefill", "nm_spmm_prefill_variant_count",
+    "nm_spmm_prefill_workspace_bytes", "nm_wait_timeouts",
     "nm_prefill_stall_selftest",
 ]
 
@@ -91,7 +92,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_spmm_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, I32, P], I32),
         "nm_spmm_variant_count": ([], I32),
         "nm_spmm_prefill": ([P, P, I64, I64, P, I64, I64, P, I64, P], I32),
-        "nm_spmm_prefill_ex": ([P, P, I64, I64, P, I64, I64, P, I64, I32, P], I32),
+        "nm_spmm_prefill_ex": ([P, P, I64, I64, P, I64, I64, P, I64, I32, I32, P, SZ, P], I32),
+        "nm_spmm_prefill_ws": ([P, P, I64, I64, P, I64, I64, P, I64, P, SZ, P], I32),
+        "nm_spmm_prefill_workspace_bytes": ([I64, I64, I64], SZ),
+        "nm_spmm_prefill_workspace_bytes_ex": ([I64, I64, I64, I32, I32], SZ),
         "nm_spmm_prefill_variant_count": ([], I32),
         "nm_wait_timeouts": ([I32], I64),
         "nm_prefill_stall_selftest": ([P, P, I64, I64, P, I64, I64, P, I64, I64, P], I32),
@@ -268,9 +272,9 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
             grid: int = 0, slices: int = 0, flags: int | None = None, cols: int | None = None):
     """Y = W X for a batch of tokens: X fp16 [batch][ldx] (first ``cols``
     columns used), Y fp16 [batch][ldy].  Batches of 1..8 run on the CUDA
-    cores (a workspace of nm_spmm_workspace_bytes(...) bytes is allocated
-    with PyTorch when needed and none is given); larger ones on the tensor
-    cores (nm_spmm_prefill)."""
+    cores, larger ones on the tensor cores (nm_spmm_prefill).  A workspace of
+    nm_spmm_workspace_bytes(...) bytes is allocated with PyTorch when needed
+    and none is given."""
     torch = _torch()
     _need_cuda(values, masks, X)
     rows = masks.shape[0]
@@ -282,8 +286,9 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
         Y = torch.empty((batch, rows), dtype=torch.float16, device=X.device)
     _need_cuda(Y, workspace)
     L = lib()
-    if workspace is None and batch <= 8:
-        need = L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, slices)
+    if workspace is None:
+        need = (L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, slices) if batch <= 8
+                else L.nm_spmm_workspace_bytes(rows, cols, batch))
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -302,10 +307,22 @@ def nm_spmm_prefill_variant_count() -> int:
     return lib().nm_spmm_prefill_variant_count()
 
 
-def nm_spmm_prefill(values, masks, X, Y=None, stream=None, variant: int = -1,
-                    cols: int | None = None):
+def nm_spmm_prefill_workspace_bytes(rows: int, cols: int, T: int, variant: int = -1,
+                                    splits: int = 0) -> int:
+    """Bytes of workspace the prefill plan needs (0: no K split)."""
+    L = lib()
+    if variant < 0 and splits <= 0:
+        return L.nm_spmm_prefill_workspace_bytes(rows, cols, T)
+    return L.nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, variant, splits)
+
+
+def nm_spmm_prefill(values, masks, X, Y=None, workspace=None, stream=None, variant: int = -1,
+                    splits: int = 0, cols: int | None = None):
     """Y = W X for a prefill-sized batch on the tensor cores: X fp16 [T][ldx]
-    (first ``cols`` columns used), Y fp16 [T][ldy]."""
+    (first ``cols`` columns used), Y fp16 [T][ldy].  ``splits`` <= 0 lets the
+    plan cut the rows' words into K slices when that fills more SMs (a
+    workspace is then allocated with PyTorch unless one is given); 1 never
+    splits."""
     torch = _torch()
     _need_cuda(values, masks, X)
     rows = masks.shape[0]
@@ -315,14 +332,24 @@ def nm_spmm_prefill(values, masks, X, Y=None, stream=None, variant: int = -1,
         raise ValueError("X and Y must have unit column stride")
     if Y is None:
         Y = torch.empty((T, rows), dtype=torch.float16, device=X.device)
-    _need_cuda(Y)
+    _need_cuda(Y, workspace)
     L = lib()
-    if variant < 0:
+    if workspace is None and splits != 1:
+        need = nm_spmm_prefill_workspace_bytes(rows, cols, T, variant, splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant < 0 and splits <= 0:
+        st = L.nm_spmm_prefill_ws(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), T,
+                                  _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes,
+                                  _stream(stream))
+    elif variant < 0 and splits == 1:
         st = L.nm_spmm_prefill(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), T,
                                _ptr(Y), Y.stride(0), _stream(stream))
     else:
         st = L.nm_spmm_prefill_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), T,
-                                  _ptr(Y), Y.stride(0), variant, _stream(stream))
+                                  _ptr(Y), Y.stride(0), variant, splits, _ptr(workspace),
+                                  ws_bytes, _stream(stream))
     _check(st, "nm_spmm_prefill")
     return Y
 

@@ -63,6 +63,8 @@ using namespace nmk;
 namespace {
 
 constexpr int64_t kMaxRows = (int64_t)1 << 31;
+constexpr int kPrefillMaxSplits = 8;   // K slices the prefill plan considers
+constexpr int kPrefillMaxSlices = 64;  // K slices a caller may ask for
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -204,8 +206,10 @@ size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int var
 int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
                size_t workspace_bytes, int variant, int grid, int slices, int flags, void* stream);
-int nm_spmm_prefill(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
-                    const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, void* stream);
+int nm_spmm_prefill_ws(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                       const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy,
+                       void* workspace, size_t workspace_bytes, void* stream);
+size_t nm_spmm_prefill_workspace_bytes(int64_t rows, int64_t cols, int64_t T);
 
 const char* nm_status_string(int status) {
   switch (status) {
@@ -411,6 +415,7 @@ size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int var
 }
 
 size_t nm_spmm_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+  if (batch > 8) return nm_spmm_prefill_workspace_bytes(rows, cols, batch);
   return nm_spmm_workspace_bytes_ex(rows, cols, batch, -1, 0);
 }
 
@@ -458,30 +463,75 @@ int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
 int nm_spmm(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, const void* X,
             int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace, size_t workspace_bytes,
             void* stream) {
-  if (batch > 8)  // beyond the CUDA-core kernel's batch: the tensor-core path, no workspace
-    return nm_spmm_prefill(values, masks, rows, cols, X, ldx, batch, Y, ldy, stream);
+  if (batch > 8)  // beyond the CUDA-core kernel's batch: the tensor-core path
+    return nm_spmm_prefill_ws(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace,
+                              workspace_bytes, stream);
   return nm_spmm_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace, workspace_bytes,
                     -1, 0, 0, NM_FLAG_PDL, stream);
 }
 
 int nm_spmm_prefill_variant_count(void) { return spmm_tc_variant_count(); }
 
+// The prefill plan (variant, K slices) for a call; variant < 0 and splits
+// <= 0 ask for the modelled choice.
+static int prefill_plan(int64_t rows, int64_t cols, int64_t T, int variant, int splits,
+                        int* v_out, int* z_out) {
+  const int words = (int)(cols / 32);
+  if (variant >= 0 && splits >= 1) {
+    *v_out = variant;
+    *z_out = splits;
+    return NM_OK;
+  }
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  spmm_tc_default_plan(rows, words, T, d.sms, variant, splits, kPrefillMaxSplits, v_out, z_out);
+  return NM_OK;
+}
+
+static bool prefill_shape_ok(int64_t rows, int64_t cols, int64_t T) {
+  return rows >= 0 && rows < kMaxRows && (rows + 127) / 128 <= 65535 && cols > 0 &&
+         cols % 32 == 0 && T >= 0 && T < kMaxRows;
+}
+
+size_t nm_spmm_prefill_workspace_bytes_ex(int64_t rows, int64_t cols, int64_t T, int variant,
+                                          int splits) {
+  if (!prefill_shape_ok(rows, cols, T) || rows == 0 || T == 0 ||
+      variant >= spmm_tc_variant_count() || splits > kPrefillMaxSlices)
+    return 0;
+  int v, z;
+  if (prefill_plan(rows, cols, T, variant, splits, &v, &z) != NM_OK) return 0;
+  return spmm_tc_workspace_bytes(rows, (int)(cols / 32), T, z);
+}
+
+size_t nm_spmm_prefill_workspace_bytes(int64_t rows, int64_t cols, int64_t T) {
+  return nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, -1, 0);
+}
+
 int nm_spmm_prefill_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                        const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, int variant,
-                       void* stream) {
+                       int splits, void* workspace, size_t workspace_bytes, void* stream) {
   if (!values || !masks || !X || !Y) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || (rows + 127) / 128 > 65535 || cols <= 0 || cols % 32 != 0 ||
-      T < 0 || T >= kMaxRows || ldx < cols || ldy < rows)
+  if (!prefill_shape_ok(rows, cols, T) || ldx < cols || ldy < rows)
     return NM_ERR_SHAPE;
-  if (variant >= spmm_tc_variant_count()) return NM_ERR_SHAPE;
+  if (variant >= spmm_tc_variant_count() || splits > kPrefillMaxSlices) return NM_ERR_SHAPE;
   if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
-      !aligned(Y, 2))
+      !aligned(Y, 2) || (workspace && !aligned(workspace, 16)))
     return NM_ERR_ALIGN;
   if (rows == 0 || T == 0) return NM_OK;
   const size_t yb = (size_t)((T - 1) * ldy + rows) * 2;
   const size_t xb = (size_t)((T - 1) * ldx + cols) * 2;
   if (overlap(Y, yb, values, (size_t)rows * cols) || overlap(Y, yb, masks, (size_t)rows * cols / 8) ||
       overlap(Y, yb, X, xb))
+    return NM_ERR_ALIAS;
+  int v, z;
+  const int st = prefill_plan(rows, cols, T, variant, splits, &v, &z);
+  if (st != NM_OK) return st;
+  const int words = (int)(cols / 32);
+  const size_t need = spmm_tc_workspace_bytes(rows, words, T, z);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return NM_ERR_WORKSPACE;
+  if (need > 0 && (overlap(workspace, need, values, (size_t)rows * cols) ||
+                   overlap(workspace, need, masks, (size_t)rows * cols / 8) ||
+                   overlap(workspace, need, X, xb) || overlap(workspace, need, Y, yb)))
     return NM_ERR_ALIAS;
   SpmmTcParams p;
   p.values = values;
@@ -491,20 +541,26 @@ int nm_spmm_prefill_ex(const void* values, const uint32_t* masks, int64_t rows, 
   p.Y = static_cast<__half*>(Y);
   p.ldy = ldy;
   p.rows = rows;
-  p.words = (int)(cols / 32);
+  p.words = words;
   p.T = T;
-  if (variant < 0) {
-    DeviceInfo d;
-    if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
-    variant = spmm_tc_default_variant(rows, T, d.sms);
-  }
-  cudaError_t e = launch_spmm_tc(p, variant, static_cast<cudaStream_t>(stream));
+  p.slices = spmm_tc_slices(words, z);
+  p.wslice = spmm_tc_slice_words(words, z);
+  p.part = static_cast<float*>(workspace);
+  cudaError_t e = launch_spmm_tc(p, v, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmm_prefill_ws(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                       const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return nm_spmm_prefill_ex(values, masks, rows, cols, X, ldx, T, Y, ldy, -1, 0, workspace,
+                            workspace_bytes, stream);
 }
 
 int nm_spmm_prefill(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                     const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, void* stream) {
-  return nm_spmm_prefill_ex(values, masks, rows, cols, X, ldx, T, Y, ldy, -1, stream);
+  return nm_spmm_prefill_ex(values, masks, rows, cols, X, ldx, T, Y, ldy, -1, 1, nullptr, 0,
+                            stream);
 }
 
 int nm_prefill_stall_selftest(const void* values, const uint32_t* masks, int64_t rows,

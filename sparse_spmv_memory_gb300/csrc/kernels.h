@@ -104,12 +104,20 @@ struct SpmmTcParams {
   int64_t rows;
   int words;                // cols / 32
   int64_t T;                // tokens
+  int slices = 1;           // K slices (> 1: fp32 partials in part, then a combine)
+  int wslice = 0;           // mask words per slice (spmm_tc_slice_words)
+  float* part = nullptr;    // fp32 [slices][T][rows] when slices > 1
   uint64_t wait_limit_ns = 0;  // bound of every in-kernel wait (0: the default)
   int stall_weights = 0;       // self-test: the weight producer issues nothing
 };
 
 int spmm_tc_variant_count();
 int spmm_tc_default_variant(int64_t rows, int64_t T, int sms);
+int spmm_tc_slice_words(int words, int splits);
+int spmm_tc_slices(int words, int splits);
+size_t spmm_tc_workspace_bytes(int64_t rows, int words, int64_t T, int splits);
+void spmm_tc_default_plan(int64_t rows, int words, int64_t T, int sms, int variant, int splits,
+                          int max_splits, int* variant_out, int* splits_out);
 int spmm_tc_block_tokens(int variant);
 cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream);
 // Number of bounded mbarrier waits that gave up since the last reset.

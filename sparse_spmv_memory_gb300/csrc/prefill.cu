@@ -76,7 +76,9 @@ constexpr uint32_t tmem_cols_for(int n) {
 // stage in the pipeline resident while the densify warps reach it.
 // MS: 0, one thread issues every stage's MMAs; 1, two threads take the even
 // and odd stages into two accumulators that the epilogue adds (K split).
-template <int NMMA, int NB, int STAGES, int MS, bool MT>
+constexpr int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
+
+template <int NMMA, int NB, int STAGES, int DG, int MS, bool MT>
 struct Layout {
   static constexpr int BN = NMMA * NB;
   static constexpr int B_BYTES = BN * ROW_BYTES;
@@ -86,9 +88,21 @@ struct Layout {
   static constexpr int M_OFF = V_OFF + STAGES * V_BYTES;
   static constexpr int MT_SLOTS = (STAGES + MW - 1 + MW - 1) / MW;
   static constexpr int M_REGION = MT ? MT_SLOTS * MT_SLOT : STAGES * M_BYTES;
-  // barriers: full, empty, afull (per stage), accum, mfull, mfree (per mask slot)
+  // Stage barriers.  A parity wait tells a phase from the one before it only,
+  // so it is exact only if the waiter itself saw the barrier's previous phase
+  // complete.  The "full" barriers therefore form a ring of lcm(STAGES, DG):
+  // all phases of one belong to stages of one densify group, which waits for
+  // each.  The "afull" barriers form a ring of 2 * STAGES when two MMA
+  // issuers split an odd STAGES, so all phases of one belong to one issuer.
+  // The "empty" barriers, one per shared-memory slot, are waited by
+  // producers that issue every stage.
+  static constexpr int FULL_RING = STAGES * DG / gcd_int(STAGES, DG);
+  static constexpr int AFULL_RING = (MS && STAGES % 2) ? 2 * STAGES : STAGES;
+  // barriers: full (ring), empty (per slot), afull (ring), accum, mfull,
+  // mfree (per mask slot)
   static constexpr int BAR_OFF = M_OFF + M_REGION;
-  static constexpr int SLOT_OFF = BAR_OFF + (3 * STAGES + 1 + 2 * MT_SLOTS) * 8;
+  static constexpr int N_BARS = FULL_RING + STAGES + AFULL_RING + 1 + 2 * MT_SLOTS;
+  static constexpr int SLOT_OFF = BAR_OFF + N_BARS * 8;
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(MS ? 2 * BN : BN);
@@ -162,9 +176,9 @@ template <int NMMA, int NB, int STAGES, int G, int DG, int DW, int MS, bool MT>
 __global__ void __launch_bounds__(threads_for(DW), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_m, const uint32_t* __restrict__ masks,
-                   __half* __restrict__ Y, int64_t rows, int words, int64_t T, int64_t ldy,
-                   uint64_t wait_limit_ns, int stall_weights) {
-  using L = Layout<NMMA, NB, STAGES, MS, MT>;
+                   __half* __restrict__ Y, float* __restrict__ part, int64_t rows, int words,
+                   int wslice, int64_t T, int64_t ldy, uint64_t wait_limit_ns, int stall_weights) {
+  using L = Layout<NMMA, NB, STAGES, DG, MS, MT>;
   static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
   static_assert(MS == 0 || G == 1, "each K-split issuer waits on each of its stages");
   static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
@@ -177,28 +191,37 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t sA = base + L::A_OFF, sB = base + L::B_OFF, sV = base + L::V_OFF,
                  sM = base + L::M_OFF, bars = base + L::BAR_OFF, slot = base + L::SLOT_OFF;
-  auto full = [&](int s) { return bars + 8u * s; };
-  auto empty = [&](int s) { return bars + 8u * (STAGES + s); };
-  auto afull = [&](int s) { return bars + 8u * (2 * STAGES + s); };
-  const uint32_t accum = bars + 8u * (3 * STAGES);
+  constexpr int FB = L::FULL_RING, AB = L::AFULL_RING;
+  // full / afull: by stage kt (rings of FB / AB); empty: by slot kt % STAGES.
+  auto full = [&](int kt) { return bars + 8u * (kt % FB); };
+  auto full_par = [&](int kt) { return (uint32_t)((kt / FB) & 1); };
+  auto empty = [&](int s) { return bars + 8u * (FB + s); };
+  auto afull = [&](int kt) { return bars + 8u * (FB + STAGES + kt % AB); };
+  auto afull_par = [&](int kt) { return (uint32_t)((kt / AB) & 1); };
+  const uint32_t accum = bars + 8u * (FB + STAGES + AB);
   // A mask box serves MW consecutive stages that may belong to different
   // densify groups, so it completes on a barrier of its own.
-  auto mfull = [&](int slot) { return bars + 8u * (3 * STAGES + 1 + slot); };
+  auto mfull = [&](int slot) { return bars + 8u * (FB + STAGES + AB + 1 + slot); };
   // ... and is released on one when every densify warp has finished its last
   // stage in the box (the stages of a box may go to different MMA issuers, so
   // no single stage's completion implies that).
-  auto mfree = [&](int slot) { return bars + 8u * (3 * STAGES + 1 + L::MT_SLOTS + slot); };
+  auto mfree = [&](int slot) {
+    return bars + 8u * (FB + STAGES + AB + 1 + L::MT_SLOTS + slot);
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t r0 = (int64_t)blockIdx.y * BM;
   const int64_t n0 = (int64_t)blockIdx.x * L::BN;
+  // K split: this block multiplies the mask words w0 .. w0 + nk - 1 (stage
+  // kt is word w0 + kt); w0 is a multiple of MW, so mask boxes stay aligned.
+  const int w0 = (int)blockIdx.z * wslice;
+  const int nk = min(words - w0, wslice);
 
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), MT ? 2 : 2 + 32);    // two expect_tx arrivals (+ 32 cp.async arrivals)
-      mbar_init(empty(s), 1);                 // tcgen05.commit
-      mbar_init(afull(s), WPG);               // one arrival per warp of the stage's group
-    }
+    for (int k = 0; k < FB; ++k)
+      mbar_init(full(k), MT ? 2 : 2 + 32);    // two expect_tx arrivals (+ 32 cp.async arrivals)
+    for (int s = 0; s < STAGES; ++s) mbar_init(empty(s), 1);  // tcgen05.commit
+    for (int k = 0; k < AB; ++k) mbar_init(afull(k), WPG);    // one arrival per warp of the group
     mbar_init(accum, MS ? 2 : 1);             // final commit of each issuer
     for (int m = 0; m < L::MT_SLOTS; ++m) {
       mbar_init(mfull(m), 1);
@@ -225,22 +248,22 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   // the slot's last.  A producer that stopped early on a timeout issued
   // nothing in the last 2 s worth waiting for.
   auto drain = [&](int last) {
-    for (int kt = last; kt >= 0 && kt > words - 1 - STAGES; --kt)
-      mbar_wait(full(kt % STAGES), (kt / STAGES) & 1, wait_limit_ns);
+    for (int kt = last; kt >= 0 && kt > nk - 1 - STAGES; --kt)
+      mbar_wait(full(kt), full_par(kt), wait_limit_ns);
   };
 
   if (warp == 0) {
     // ---- X producer: the token tile of each stage -------------------------
     if (lane == 0) {
       int last = -1;
-      for (int kt = 0; kt < words; ++kt) {
+      for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
         if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns)) break;
-        mbar_arrive_expect_tx(full(s), L::B_BYTES);
+        mbar_arrive_expect_tx(full(kt), L::B_BYTES);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
-          tma_load_2d(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES, &tm_x, kt * BK,
-                      (int)(n0 + j * NMMA), full(s));
+          tma_load_2d(sB + s * L::B_BYTES + j * NMMA * ROW_BYTES, &tm_x, (w0 + kt) * BK,
+                      (int)(n0 + j * NMMA), full(kt));
         last = kt;
       }
       drain(last);
@@ -255,15 +278,15 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     // wait then runs out and the block tears down without storing Y.
     if ((!MT || lane == 0) && !stall_weights) {
       int last = -1;
-      for (int kt = 0; kt < words; ++kt) {
+      for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % STAGES, u = kt / STAGES;
         int ok = 1;
         if (u > 0 && lane == 0) ok = mbar_wait(empty(s), (u - 1) & 1, wait_limit_ns);
         if (!MT) ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(full(s), V_BYTES);
-          tma_load_2d(sV + s * V_BYTES, &tm_v, kt * 16, (int)r0, full(s));
+          mbar_arrive_expect_tx(full(kt), V_BYTES);
+          tma_load_2d(sV + s * V_BYTES, &tm_v, (w0 + kt) * 16, (int)r0, full(kt));
         }
         if (!MT) {
 #pragma unroll
@@ -271,10 +294,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
             const int rr = lane + 32 * i;
             const int64_t gr = r0 + rr;
             const bool in = gr < rows;
-            cp_async_4(sM + s * M_BYTES + 4u * rr, masks + (in ? gr : 0) * words + kt,
+            cp_async_4(sM + s * M_BYTES + 4u * rr, masks + (in ? gr : 0) * words + w0 + kt,
                        in ? 4u : 0u);
           }
-          cp_async_arrive_noinc(full(s));
+          cp_async_arrive_noinc(full(kt));
         }
         last = kt;
       }
@@ -289,13 +312,13 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     // release waited for is always the previous box's.
     if (MT && lane == 0 && !stall_weights) {
       int nbox = 0;
-      for (int kt = 0; kt < words; kt += MW) {
+      for (int kt = 0; kt < nk; kt += MW) {
         const int b = kt / MW, ms = b % L::MT_SLOTS;
         if (b >= L::MT_SLOTS &&
             !mbar_wait(mfree(ms), ((b / L::MT_SLOTS) - 1) & 1, wait_limit_ns))
           break;
         mbar_arrive_expect_tx(mfull(ms), MT_SLOT);
-        tma_load_2d(sM + ms * MT_SLOT, &tm_m, kt, (int)r0, mfull(ms));
+        tma_load_2d(sM + ms * MT_SLOT, &tm_m, w0 + kt, (int)r0, mfull(ms));
         nbox = kt / MW + 1;
       }
       const int b0 = nbox > L::MT_SLOTS ? nbox - L::MT_SLOTS : 0;  // boxes still in flight
@@ -318,9 +341,9 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       constexpr uint32_t idesc = idesc_f16_f32(BM, NMMA);
       const int k0 = MS ? role : 0, kstep = MS ? 2 : G;
       const uint32_t dacc = tmem_base + (uint32_t)(MS && role ? L::BN : 0);
-      for (int kt = k0; kt < words; kt += kstep) {
-        const int last = MS ? kt : (kt + G - 1 < words ? kt + G - 1 : words - 1);
-        if (!mbar_wait(afull(last % STAGES), (last / STAGES) & 1, wait_limit_ns)) break;
+      for (int kt = k0; kt < nk; kt += kstep) {
+        const int last = MS ? kt : (kt + G - 1 < nk ? kt + G - 1 : nk - 1);
+        if (!mbar_wait(afull(last), afull_par(last), wait_limit_ns)) break;
         tc_fence_after_sync();
         for (int k = kt; k <= last; ++k) {
           const int s = k % STAGES;
@@ -334,7 +357,11 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
               mma_f16(dacc + (uint32_t)(j * NMMA), ad, bd, idesc, (k != k0) || (ks != 0));
             }
           }
-          mma_commit(empty(s));
+          // Only a slot that a producer refills gets its release: no one
+          // waits for the last STAGES stages', and a commit's arrival is not
+          // ordered with the accum commit's, so it could land after this
+          // block ended, in the barriers of the next block on the SM.
+          if (k + STAGES < nk) mma_commit(empty(s));
         }
       }
       mma_commit(accum);  // also after an early exit: completes once issued MMAs finish
@@ -346,9 +373,9 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
     const int grp = dw / WPG, wg = dw % WPG;
     bool ok = true;
     int box = -1;  // mask box this warp last waited for
-    for (int kt = grp; kt < words; kt += DG) {
-      const int s = kt % STAGES, u = kt / STAGES;
-      bool got = mbar_wait(full(s), u & 1, wait_limit_ns);
+    for (int kt = grp; kt < nk; kt += DG) {
+      const int s = kt % STAGES;
+      bool got = mbar_wait(full(kt), full_par(kt), wait_limit_ns);
       if (MT && kt / MW != box) {
         // The box's slot is refilled only after every densify warp released
         // it, so the phase this warp sees here is this box's.
@@ -366,7 +393,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(afull(s));
+        mbar_arrive(afull(kt));
         // This warp's last stage in the mask box: it has read the box (its
         // loads precede the release-arrive), so the slot may be refilled.
         if (MT && kt + DG >= MW * (kt / MW + 1)) mbar_arrive(mfree((kt / MW) % L::MT_SLOTS));
@@ -387,7 +414,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
         uint32_t v[32];
         tmem_ld_32(tbase + (uint32_t)c0, v);
         tmem_ld_wait();
-        if (MS && words > 1) {  // the odd stages' accumulator (none when words == 1)
+        if (MS && nk > 1) {  // the odd stages' accumulator (none when nk == 1)
           uint32_t w[32];
           tmem_ld_32(tbase + (uint32_t)(L::BN + c0), w);
           tmem_ld_wait();
@@ -395,7 +422,14 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
           for (int i = 0; i < 32; ++i)
             v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(w[i]));
         }
-        if (row_ok) {
+        if (row_ok && part) {  // K split: this slice's fp32 sums, [slice][T][rows]
+          float* pz = part + (int64_t)blockIdx.z * T * rows + r;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int64_t t = n0 + c0 + i;
+            if (t < T) pz[t * rows] = __uint_as_float(v[i]);
+          }
+        } else if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int64_t t = n0 + c0 + i;
@@ -460,7 +494,7 @@ static bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t 
 
 template <int NMMA, int NB, int STAGES, int G, int DG, int DW, int MS, bool MT>
 static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
-  using L = Layout<NMMA, NB, STAGES, MS, MT>;
+  using L = Layout<NMMA, NB, STAGES, DG, MS, MT>;
   CUtensorMap tm_v, tm_x, tm_m;
   memset(&tm_m, 0, sizeof(tm_m));
   if (MT && !encode_2d(&tm_m, p.masks, (uint64_t)p.words, (uint64_t)p.rows,
@@ -481,15 +515,42 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = 1;
   }
-  const dim3 grid((unsigned)((p.T + L::BN - 1) / L::BN), (unsigned)((p.rows + BM - 1) / BM));
+  const int wslice = p.slices > 1 ? p.wslice : p.words;
+  const dim3 grid((unsigned)((p.T + L::BN - 1) / L::BN), (unsigned)((p.rows + BM - 1) / BM),
+                  (unsigned)(p.slices > 1 ? p.slices : 1));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads_for(DW));
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = stream;
   const uint64_t limit = p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
-  return cudaLaunchKernelEx(&cfg, k, tm_v, tm_x, tm_m, p.masks, p.Y, p.rows, p.words, p.T,
-                            p.ldy, limit, p.stall_weights);
+  float* part = p.slices > 1 ? p.part : nullptr;
+  return cudaLaunchKernelEx(&cfg, k, tm_v, tm_x, tm_m, p.masks, p.Y, part, p.rows, p.words,
+                            wslice, p.T, p.ldy, limit, p.stall_weights);
+}
+
+// Y[t][r] = fp16(sum over slices z, in increasing z, of part[z][t][r]): the
+// K split's fixed-order combine (one rounding, no atomics).
+__global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict__ part,
+                                                         int slices, int64_t T, int64_t rows,
+                                                         __half* __restrict__ Y, int64_t ldy) {
+  const int64_t plane = T * rows;
+  for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+         r += (int64_t)gridDim.x * blockDim.x) {
+      const float* q = part + t * rows + r;
+      float acc = q[0];
+      for (int z = 1; z < slices; ++z) acc += q[z * plane];
+      Y[t * ldy + r] = __float2half_rn(acc);
+    }
+  }
+}
+
+static cudaError_t launch_splitk_sum(const SpmmTcParams& p, cudaStream_t stream) {
+  const int64_t bx = (p.rows + 255) / 256;
+  const dim3 grid((unsigned)(bx < 65535 ? bx : 65535), (unsigned)(p.T < 65535 ? p.T : 65535));
+  splitk_sum_kernel<<<grid, 256, 0, stream>>>(p.part, p.slices, p.T, p.rows, p.Y, p.ldy);
+  return cudaGetLastError();
 }
 
 // Mask words by TMA when the mask array allows it (16-byte aligned, row pitch
@@ -505,36 +566,93 @@ static cudaError_t launch_tc(const SpmmTcParams& p, cudaStream_t stream) {
 
 int spmm_tc_variant_count() { return tc::kVariantCount; }
 
-// The variant that minimises (waves of blocks) x (time of one block), with
-// each variant's time per 32-column stage measured on GB300 over the
-// decoder-layer shapes (ns, one block per SM): 512 tokens 441 (5 stages),
-// 256 tokens 319 (7), 128 tokens 232 (10), 64 tokens 218 (12).  A larger token tile does
-// more work per stage, a smaller one fills more SMs when rows are few.
-int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
-  static const struct {
-    int variant, tokens;
-    double ns_per_stage;
-  } cand[] = {{4, 512, 441.0}, {1, 256, 319.0}, {2, 128, 232.0}, {3, 64, 218.0}};
+// Words per K slice when a row of `words` mask words is cut into at most
+// `splits` slices: a multiple of four (one mask box), so every slice but the
+// last is whole boxes.  The slice count is then ceil(words / slice).
+int spmm_tc_slice_words(int words, int splits) {
+  if (splits <= 1 || words <= 4) return words;
+  const int w = (words + splits - 1) / splits;
+  const int r = (w + 3) / 4 * 4;
+  return r < words ? r : words;
+}
+
+int spmm_tc_slices(int words, int splits) {
+  const int w = spmm_tc_slice_words(words, splits);
+  return (words + w - 1) / w;
+}
+
+size_t spmm_tc_workspace_bytes(int64_t rows, int words, int64_t T, int splits) {
+  const int z = spmm_tc_slices(words, splits);
+  return z > 1 ? (size_t)z * (size_t)T * (size_t)rows * sizeof(float) : 0;
+}
+
+// Time model of a plan (variant, K slices), in ns: waves of blocks x (the
+// slice's stages x the variant's time per 32-column stage + a block's fixed
+// cost), plus, when split, the combine (a launch and its traffic).  Times per
+// stage measured on GB300 over the decoder-layer shapes, one block per SM:
+// 512 tokens 441 (5 stages), 256 tokens 319 (7), 128 tokens 232 (10), 64
+// tokens 218 (12).  A larger token tile does more work per stage; a smaller
+// one, or a K split, fills more SMs when rows (or tokens) are few.
+namespace {
+struct Cand {
+  int variant, tokens;
+  double ns_per_stage;
+};
+constexpr Cand kCand[] = {{4, 512, 441.0}, {1, 256, 319.0}, {2, 128, 232.0}, {3, 64, 218.0}};
+constexpr double kBlockNs = 3000.0;        // prologue, pipeline fill, epilogue
+constexpr double kCombineNs = 2500.0;      // the combine kernel's launch and ramp
+constexpr double kCombineBytesPerNs = 5000.0;
+constexpr size_t kMaxSplitBytes = (size_t)256 << 20;
+
+double plan_ns(const Cand& c, int64_t rows, int words, int64_t T, int sms, int splits) {
+  const int64_t tiles = ((rows + 127) / 128) * ((T + c.tokens - 1) / c.tokens);
+  const int z = spmm_tc_slices(words, splits);
+  const int64_t waves = (tiles * z + sms - 1) / sms;
+  double t = (double)waves * (spmm_tc_slice_words(words, splits) * c.ns_per_stage + kBlockNs);
+  if (z > 1)
+    t += kCombineNs + (double)(4 * z + 4 * z + 2) * (double)T * (double)rows / kCombineBytesPerNs;
+  return t;
+}
+}  // namespace
+
+// The plan of least modelled time.  variant >= 0 fixes the variant; splits
+// >= 1 fixes the slice request (1: no split); max_splits bounds the search.
+void spmm_tc_default_plan(int64_t rows, int words, int64_t T, int sms, int variant, int splits,
+                          int max_splits, int* variant_out, int* splits_out) {
   if (sms < 1) sms = 1;
-  const int64_t row_tiles = (rows + 127) / 128;
-  int best = 3;
+  int best_v = variant >= 0 ? variant : 3, best_z = 1;
   double best_t = 0.0;
-  for (const auto& c : cand) {
-    const int64_t blocks = row_tiles * ((T + c.tokens - 1) / c.tokens);
-    const double t = (double)((blocks + sms - 1) / sms) * c.ns_per_stage;
-    if (best_t == 0.0 || t < best_t * 0.97) {  // prefer the earlier (larger) tile on near-ties
-      best = c.variant;
-      best_t = t;
+  for (const auto& c : kCand) {
+    if (variant >= 0 && c.variant != variant) continue;
+    const int lo = splits >= 1 ? splits : 1, hi = splits >= 1 ? splits : max_splits;
+    for (int z = lo; z <= hi; ++z) {
+      if (z > 1 && (spmm_tc_slices(words, z) != z ||
+                    spmm_tc_workspace_bytes(rows, words, T, z) > kMaxSplitBytes))
+        continue;
+      const double t = plan_ns(c, rows, words, T, sms, z);
+      if (best_t == 0.0 || t < best_t * 0.97) {  // prefer the earlier (larger tile, fewer slices)
+        best_v = c.variant;
+        best_z = z;
+        best_t = t;
+      }
     }
   }
-  return best;
+  if (variant >= 0 && best_t == 0.0) best_z = splits >= 1 ? splits : 1;  // variant 0: not modelled
+  *variant_out = best_v;
+  *splits_out = best_z;
+}
+
+int spmm_tc_default_variant(int64_t rows, int64_t T, int sms) {
+  int v, z;
+  spmm_tc_default_plan(rows, 32, T, sms, -1, 1, 1, &v, &z);
+  return v;
 }
 
 int spmm_tc_block_tokens(int variant) {
   return tc::kVariants[variant].nmma * tc::kVariants[variant].nb;
 }
 
-cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
+static cudaError_t launch_spmm_tc_main(const SpmmTcParams& p, int variant, cudaStream_t stream) {
   switch (variant) {
     case 0: return tc::launch_tc<256, 2, 4, 1, 2, 16, 0>(p, stream);
     case 1: return tc::launch_tc<256, 1, 7, 1, 2, 16, 1>(p, stream);
@@ -543,6 +661,12 @@ cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stre
     case 4: return tc::launch_tc<256, 2, 5, 1, 4, 16, 0>(p, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_spmm_tc(const SpmmTcParams& p, int variant, cudaStream_t stream) {
+  cudaError_t e = launch_spmm_tc_main(p, variant, stream);
+  if (e != cudaSuccess || p.slices <= 1) return e;
+  return tc::launch_splitk_sum(p, stream);
 }
 
 cudaError_t read_wait_timeouts(unsigned long long* count, int reset) {

@@ -67,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) {
+    if ((int64_t)(global_timer_ns() - t0) > (int64_t)limit_ns) {  // a step back is no timeout
       atomicAdd(&g_wait_timeouts, 1ull);
       return false;
     }

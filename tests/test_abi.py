@@ -60,6 +60,13 @@ def test_host_only_entry_points():
     assert nm.nm_values_bytes(4, 48) == 0 and nm.nm_masks_bytes(-1, 32) == 0
     assert nm.nm_spmv_workspace_bytes(4096, 4096) == 0
     assert nm.nm_spmv_variant_count() >= 1 and nm.dense_gemv_variant_count() >= 1
+    # explicit prefill plans are sized on the host: K slices of whole boxes of
+    # four mask words, fp32 [slices][T][rows]
+    assert nm.nm_spmm_prefill_workspace_bytes(8192, 8192, 64, 3, 2) == 2 * 64 * 8192 * 4
+    assert nm.nm_spmm_prefill_workspace_bytes(300, 1056, 77, 1, 5) == 5 * 77 * 300 * 4  # 8,8,8,8,1
+    assert nm.nm_spmm_prefill_workspace_bytes(300, 1056, 77, 1, 1) == 0
+    assert nm.nm_spmm_prefill_workspace_bytes(64, 128, 16, 0, 8) == 0     # one box: no split
+    assert nm.nm_spmm_prefill_workspace_bytes(300, 1056, 77, 1, 65) == 0  # beyond 64: refused
 
 
 def test_library_has_no_oracle_dependency():

@@ -129,18 +129,37 @@ def test_prefill_argument_errors(nm):
     assert L.nm_spmm_prefill(P(v) + 2, P(m), 64, 64, P(X), 64, 16, P(Y), 64, st) == 4
     assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X) + 2, 64, 16, P(Y), 64, st) == 4
     assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 64, 16, P(X), 64, st) == 7   # Y aliases X
-    assert L.nm_spmm_prefill_ex(P(v), P(m), 64, 64, P(X), 64, 16, P(Y), 64, 99, st) == 2
+    assert L.nm_spmm_prefill_ex(P(v), P(m), 64, 64, P(X), 64, 16, P(Y), 64, 99, 1, None, 0,
+                                st) == 2                                        # variant
+    assert L.nm_spmm_prefill_ex(P(v), P(m), 64, 64, P(X), 64, 16, P(Y), 64, 3, 65, None, 0,
+                                st) == 2                                        # splits > 64
     assert L.nm_spmm_prefill(P(v), P(m), 64, 64, P(X), 64, 0, P(Y), 64, st) == 0    # T == 0
+    # a K split needs its workspace (256 columns = 8 words: two slices of four)
+    v2 = torch.zeros(64 * 128, dtype=torch.float16, device="cuda")
+    m2 = torch.zeros(64 * 8, dtype=torch.int32, device="cuda")
+    X2 = torch.zeros((16, 256), dtype=torch.float16, device="cuda")
+    need = L.nm_spmm_prefill_workspace_bytes_ex(64, 256, 16, 3, 2)
+    assert need == 2 * 16 * 64 * 4
+    ws = torch.zeros(need + 16, dtype=torch.uint8, device="cuda")
+    args = (P(v2), P(m2), 64, 256, P(X2), 256, 16, P(Y), 64, 3, 2)
+    assert L.nm_spmm_prefill_ex(*args, None, 0, st) == 5                       # no workspace
+    assert L.nm_spmm_prefill_ex(*args, P(ws), need - 4, st) == 5              # short
+    assert L.nm_spmm_prefill_ex(*args, P(ws) + 8, need, st) == 4              # misaligned
+    assert L.nm_spmm_prefill_ex(*args, P(Y), need, st) == 7                   # aliases Y
+    assert L.nm_spmm_prefill_ex(*args, P(ws), need, st) == 0
     torch.cuda.synchronize()
 
 
-FULL = [(57344, 8192, 2048, (2, 4)), (10240, 8192, 1000, (16, 32)), (8192, 28672, 520, (8, 16))]
+FULL = [(57344, 8192, 2048, (2, 4)), (10240, 8192, 1000, (16, 32)), (8192, 28672, 520, (8, 16)),
+        (8192, 8192, 64, (2, 4)), (8192, 28672, 200, (4, 8))]
 
 
 @pytest.mark.parametrize("rows,cols,T,pat", FULL)
 def test_prefill_full_size_sampled(nm, orc, rows, cols, T, pat):
-    """Decoder-layer shapes at prefill lengths: sampled rows (tile edges
-    included) of sampled tokens (first and last included) against the oracle."""
+    """Decoder-layer shapes at prefill lengths, in the library's default plan
+    (the short prompts on the 8192-row matrices take a K split): sampled rows
+    (tile edges included) of sampled tokens (first and last included)
+    against the oracle."""
     N, M = pat
     W = synth.weights(rows, cols, 0, synth.stream_id(71, rows, cols, 0))
     X = synth.normal_f16((T, cols), 0, synth.stream_id(71, rows, cols, 1), synth.X_SIGMA)
@@ -162,6 +181,94 @@ def test_prefill_full_size_sampled(nm, orc, rows, cols, T, pat):
         y_ref, s = orc.spmv_rows_f64(hv, hm, cols, X[t], row_ids)
         got = f16_to_f64(Yh[t, row_ids])
         assert np.all(np.abs(got - y_ref) <= oracle.tolerance(s)), f"token {t}"
+
+
+def slices_of(words, splits):
+    """Slice count the library derives from a split request: slices of
+    ceil(words / splits) words rounded up to whole mask boxes of four."""
+    if splits <= 1 or words <= 4:
+        return 1
+    per = -(-words // splits)              # ceil(words / splits)
+    per = min(words, -(-per // 4) * 4)     # whole boxes of four words
+    return -(-words // per)
+
+
+SPLIT_SHAPES = [(300, 1056, 77), (257, 2048, 600), (64, 4096, 9), (128, 1024, 64), (200, 416, 130)]
+
+
+@pytest.mark.parametrize("rows,cols,T", SPLIT_SHAPES)
+def test_prefill_k_split_exact(nm, orc, rows, cols, T):
+    """Explicit K splits for every variant -- slices of whole mask boxes, a
+    ragged last slice, odd word counts (the cp.async mask path), up to one
+    slice per box -- with the partial sums combined in slice order: bit-exact
+    against the oracle on exact-arithmetic inputs, and repeatable."""
+    W, X = gen(rows, cols, T, 14, exact=True)
+    ov, om, v, m = dev_packed(orc, W, 2, 4)
+    y_ref, _ = oracle_Y(orc, ov, om, cols, X)
+    want = orc.round_f16(y_ref).reshape(y_ref.shape)
+    Xd = to_dev(X)
+    words = cols // 32
+    for variant in range(nm.nm_spmm_prefill_variant_count()):
+        for splits in sorted({2, 3, 5, min(words, 64)}):
+            z = slices_of(words, splits)
+            need = nm.nm_spmm_prefill_workspace_bytes(rows, cols, T, variant, splits)
+            assert need == (z * T * rows * 4 if z > 1 else 0), (variant, splits)
+            got = from_dev(nm.nm_spmm_prefill(v, m, Xd, variant=variant, splits=splits))
+            bad = np.argwhere(got != want)
+            assert bad.size == 0, (f"variant {variant} splits {splits} ({z} slices): "
+                                   f"{len(bad)} mismatches, first {bad[:3].tolist()}")
+    a = nm.nm_spmm_prefill(v, m, Xd, variant=3, splits=5)
+    b = nm.nm_spmm_prefill(v, m, Xd, variant=3, splits=5)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert nm.nm_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("N,M", PATTERNS)
+def test_prefill_default_plan_splits_few_row_tiles(nm, orc, N, M):
+    """Eight row tiles and 64 tokens fill few of the SMs: the default plan
+    cuts K (it needs a workspace), and its result is within the tolerance of
+    the oracle, like the unsplit call's."""
+    rows, cols, T = 1024, 8192, 64
+    assert nm.nm_spmm_prefill_workspace_bytes(rows, cols, T) > 0
+    W, X = gen(rows, cols, T, 15 + N)
+    ov, om, v, m = dev_packed(orc, W, N, M)
+    y_ref, s = oracle_Y(orc, ov, om, cols, X)
+    Xd = to_dev(X)
+    for splits in (0, 1):
+        Y = f16_to_f64(from_dev(nm.nm_spmm_prefill(v, m, Xd, splits=splits)))
+        err = np.abs(Y - y_ref)
+        assert np.all(err <= oracle.tolerance(s)), (splits, float((err / oracle.tolerance(s)).max()))
+    assert nm.nm_wait_timeouts() == 0
+
+
+def test_prefill_many_short_blocks_repeatable(nm, orc):
+    """Tens of thousands of short blocks (eight K slices of 16 words on the
+    512-token tile, 1792 blocks a call, 24 calls): every block's pipeline
+    drains cleanly before the next block takes its SM, so no wait runs out
+    and every call returns the same bits -- those of the unsplit call on
+    exact-arithmetic inputs, and within the tolerance of the oracle on
+    sampled rows."""
+    rows, cols, T = 28672, 4096, 512
+    W, X = gen(rows, cols, T, 16, exact=True)
+    Wd = to_dev(W)
+    v, m = nm.nm_pack(Wd, 2, 4)
+    del Wd
+    Xd = to_dev(X)
+    ws = torch.empty(nm.nm_spmm_prefill_workspace_bytes(rows, cols, T, 4, 8), dtype=torch.uint8,
+                     device="cuda")
+    ref = nm.nm_spmm_prefill(v, m, Xd, variant=4, splits=1)
+    Y = torch.empty_like(ref)
+    nm.nm_wait_timeouts(reset=True)
+    for _ in range(24):
+        nm.nm_spmm_prefill(v, m, Xd, Y=Y, workspace=ws, variant=4, splits=8)
+        assert torch.equal(Y.view(torch.int16), ref.view(torch.int16))
+    assert nm.nm_wait_timeouts() == 0
+    hv, hm = from_dev(v), from_dev(m)
+    row_ids = np.array([0, 127, 128, 14335, rows - 1], dtype=np.int64)
+    Yh = from_dev(Y)
+    for t in (0, T - 1):
+        y_ref, s = orc.spmv_rows_f64(hv, hm, cols, X[t], row_ids)
+        assert np.all(np.abs(f16_to_f64(Yh[t, row_ids]) - y_ref) <= oracle.tolerance(s))
 
 
 def test_prefill_nonfinite_activation_is_dense_semantics(nm, orc):
@@ -188,7 +295,8 @@ def test_prefill_nonfinite_activation_is_dense_semantics(nm, orc):
 
 
 def test_nm_spmm_beyond_eight_tokens_takes_the_tensor_core_path(nm, orc):
-    """nm_spmm with batch > 8 is served by nm_spmm_prefill: the same bits."""
+    """nm_spmm with batch > 8 is served by the tensor-core path in its default
+    plan (with the workspace nm_spmm_workspace_bytes names): the same bits."""
     rows, cols, T = 300, 2048, 12
     W, X = gen(rows, cols, T, 12)
     ov, om, v, m = dev_packed(orc, W, 8, 16)
@@ -249,8 +357,10 @@ def test_prefill_randomised_shapes_bit_exact(nm, orc):
         want = orc.round_f16(y_ref).reshape(y_ref.shape)
         Xd = to_dev(X)
         for variant in range(nm.nm_spmm_prefill_variant_count()):
-            got = from_dev(nm.nm_spmm_prefill(v, m, Xd, variant=variant))
-            bad = np.argwhere(got != want)
-            assert bad.size == 0, (f"rows {rows} cols {cols} T {T} {N}:{M} variant {variant}: "
-                                   f"{len(bad)} mismatches, first {bad[:3].tolist()}")
+            for splits in (1, 2 + (ci + variant) % 9):
+                got = from_dev(nm.nm_spmm_prefill(v, m, Xd, variant=variant, splits=splits))
+                bad = np.argwhere(got != want)
+                assert bad.size == 0, (f"rows {rows} cols {cols} T {T} {N}:{M} variant {variant} "
+                                       f"splits {splits}: {len(bad)} mismatches, first "
+                                       f"{bad[:3].tolist()}")
     assert nm.nm_wait_timeouts() == 0

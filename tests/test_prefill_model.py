@@ -15,6 +15,8 @@ GPU, that:
   * the shared-memory layout of each kernel variant fits a GB300 block and
     keeps the swizzled tiles 1024-byte aligned.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -58,13 +60,16 @@ def mt_slots(stages):
 
 
 def layout(nmma, nb, stages, mt=True):
+    vi = VARIANTS.index((nmma, nb, stages))
+    full_ring, afull_ring = barrier_rings(stages, DENSIFY_GROUPS[vi], MMA_SPLIT[vi])
     bn = nmma * nb
     a_off = 0
     b_off = a_off + stages * A_BYTES
     v_off = b_off + stages * bn * ROW_BYTES
     m_off = v_off + stages * V_BYTES
     bar_off = m_off + (mt_slots(stages) * MT_SLOT if mt else stages * M_BYTES)
-    slot_off = bar_off + (3 * stages + 1 + mt_slots(stages)) * 8
+    n_bars = full_ring + stages + afull_ring + 1 + 2 * mt_slots(stages)
+    slot_off = bar_off + n_bars * 8
     return dict(BN=bn, B_OFF=b_off, V_OFF=v_off, M_OFF=m_off, BAR_OFF=bar_off,
                 BYTES=slot_off + 16, SMEM=slot_off + 16 + 1024)
 
@@ -190,82 +195,205 @@ def test_densify_groups_split_stages_and_read_every_mask_box():
         assert sorted(seen) == list(range(words))
 
 
-def _run_pipeline(stages, dg, split, words, rng, warps_per_group=2):
-    """Event model of one block's barrier protocol with masks by TMA: the X/W
-    producer (stage kt once the MMAs of stage kt - STAGES are done), the mask
-    producer (box b once every densify warp released box b - slots), densify
-    warps (group g takes stages g, g + DG, ...; each needs the stage's tiles
-    and its mask box in its slot, and releases the box after its last stage
-    there) and one or two MMA issuers (with the K split: even / odd stages).
-    Actors move in random order.  Asserts that no slot is refilled while a
-    warp still has to read the box it holds, and that the block never
-    deadlocks."""
+class _Barrier:
+    """An mbarrier: a phase completes when its expected arrivals are in and
+    its pending transaction bytes (here: copies) have landed.  A parity wait
+    passes when the current phase's parity differs from the one named -- so
+    on a fresh barrier a wait for parity 1 passes at once, and a waiter that
+    is a phase ahead of the barrier passes too early.  Arrivals carry the
+    stage they belong to, so a phase that mixes two stages is caught."""
+
+    def __init__(self, count):
+        self.count, self.arrived, self.tx, self.completed, self.tags = count, 0, 0, 0, []
+
+    def arrive(self, tag=None, expect=0):
+        self.arrived += 1
+        self.tx += expect
+        if tag is not None:
+            self.tags.append(tag)
+        self._check()
+
+    def land(self):
+        self.tx -= 1
+        self._check()
+
+    def _check(self):
+        if self.arrived == self.count and self.tx == 0:
+            assert len(set(self.tags)) <= 1, f"one phase collected arrivals of stages {self.tags}"
+            self.completed += 1
+            self.arrived, self.tags = 0, []
+
+
+def barrier_rings(stages, dg, split):
+    """Lengths of the kernel's stage-barrier rings.  A parity wait is exact
+    only when the waiter itself waited for the barrier's previous phase, so
+    each "full" barrier serves stages of one densify group only (a ring of
+    lcm(STAGES, DG) barriers, not one per shared-memory slot), and each
+    "afull" barrier stages of one MMA issuer only (2 * STAGES barriers when
+    two issuers split an odd number of stages)."""
+    full = stages * dg // math.gcd(stages, dg)
+    afull = 2 * stages if split and stages % 2 else stages
+    return full, afull
+
+
+def _run_block(stages, dg, split, words, rng, wpg=2, rings=True, commit_last=False):
+    """Event model of one block of the prefill kernel, masks by TMA: an X
+    producer and a W producer (stage kt after the MMAs of stage kt - STAGES
+    released its slot), the mask producer (box b after every densify warp
+    released box b - slots), DG groups of densify warps (group g takes stages
+    g, g + DG, ...), one or two MMA issuers (with the K split: even / odd
+    stages), and the copies and MMAs as asynchronous events that complete in
+    any order (the MMAs of one issuer in issue order).  Actors and events run
+    in random order with real parity-wait semantics.  Checks: every wait
+    passes only once the phase it means has completed; every reader sees the
+    stage it expects in each slot (values, mask box, densified tile, token
+    tile); no slot is overwritten before its last reader; the block always
+    completes.  `rings`: the kernel's barrier rings; False indexes every stage
+    barrier by its shared-memory slot."""
+    S, MWn = stages, MW
+    FB, AB = barrier_rings(stages, dg, split) if rings else (stages, stages)
     slots = mt_slots(stages)
-    nbox = words // MW
-    nwarps = dg * warps_per_group
-    full, mma_done = [False] * words, [False] * words
-    afull, released = [0] * words, [0] * nbox
-    slot_box = [-1] * slots
-    xw_next, mask_next = 0, 0
-    warp_next = [w // warps_per_group for w in range(nwarps)]
+    nbox = words // MWn
     issuers = 2 if split else 1
-    mma_next = list(range(issuers))
+    bars = {}
+    for st in range(S):
+        bars[f"empty{st}"] = _Barrier(1)
+    for b in range(FB):
+        bars[f"full{b}"] = _Barrier(2)
+    for b in range(AB):
+        bars[f"afull{b}"] = _Barrier(wpg)
+    for sl in range(slots):
+        bars[f"mfull{sl}"] = _Barrier(1)
+        bars[f"mfree{sl}"] = _Barrier(dg * wpg)
+    bars["accum"] = _Barrier(issuers)
+    xslot, vslot, mslot = [-1] * S, [-1] * S, [-1] * slots
+    aslot = [[-1] * wpg for _ in range(S)]
+    mma_done = [False] * words
+    dens_next = {}
+    events = []                      # pending copies: (kind, index)
+    mma_q = [[] for _ in range(issuers)]
 
-    def still_needs(w, b):
-        return any(k // MW == b for k in range(warp_next[w], words, dg))
+    def wait(bar, parity, phase):
+        return ("wait", bar, parity, phase)
 
-    while not all(mma_done):
-        moves = []
-        if xw_next < words and (xw_next < stages or mma_done[xw_next - stages]):
-            moves.append(("xw",))
-        if mask_next < nbox and (mask_next < slots or released[mask_next - slots] == nwarps):
-            moves.append(("mask",))
-        for w in range(nwarps):
-            kt = warp_next[w]
-            if kt < words and full[kt] and slot_box[(kt // MW) % slots] == kt // MW:
-                moves.append(("dens", w))
-        for i in range(issuers):
-            kt = mma_next[i]
-            if kt < words and afull[kt] == warps_per_group:
-                moves.append(("mma", i))
-        assert moves, "deadlock"
-        m = moves[rng.integers(len(moves))]
-        if m[0] == "xw":
-            full[xw_next] = True
-            xw_next += 1
-        elif m[0] == "mask":
-            s = mask_next % slots
-            if slot_box[s] >= 0:
-                assert not any(still_needs(w, slot_box[s]) for w in range(nwarps))
-            slot_box[s] = mask_next
-            mask_next += 1
-        elif m[0] == "dens":
-            w = m[1]
-            kt = warp_next[w]
-            afull[kt] += 1
-            if kt + dg >= MW * (kt // MW + 1):   # this warp's last stage in the box
-                released[kt // MW] += 1
-            warp_next[w] += dg
+    def producer(kind):
+        for kt in range(words):
+            st, u = kt % S, kt // S
+            if u > 0:
+                yield wait(f"empty{st}", (u - 1) & 1, u - 1)
+            bars[f"full{kt % FB}"].arrive(expect=1, tag=kt)
+            events.append((kind, kt))
+        for kt in range(words - 1, max(-1, words - 1 - S), -1):
+            yield wait(f"full{kt % FB}", (kt // FB) & 1, kt // FB)
+
+    def mask_producer():
+        for b in range(nbox):
+            sl = b % slots
+            if b >= slots:
+                yield wait(f"mfree{sl}", ((b // slots) - 1) & 1, (b // slots) - 1)
+            bars[f"mfull{sl}"].arrive(expect=1)
+            events.append(("M", b))
+        for b in range(max(0, nbox - slots), nbox):
+            yield wait(f"mfull{b % slots}", (b // slots) & 1, b // slots)
+
+    def densify(g, wi):
+        key = (g, wi)
+        box = -1
+        for kt in range(g, words, dg):
+            dens_next[key] = kt
+            st = kt % S
+            yield wait(f"full{kt % FB}", (kt // FB) & 1, kt // FB)
+            if kt // MWn != box:
+                box = kt // MWn
+                yield wait(f"mfull{box % slots}", (box // slots) & 1, box // slots)
+            assert vslot[st] == kt, f"densify of stage {kt} read the values of stage {vslot[st]}"
+            assert mslot[box % slots] == box, f"stage {kt} read mask box {mslot[box % slots]}"
+            aslot[st][wi] = kt
+            yield ("step",)
+            bars[f"afull{kt % AB}"].arrive(tag=kt)
+            if kt + dg >= MWn * (kt // MWn + 1):
+                bars[f"mfree{box % slots}"].arrive(tag=box)
+        dens_next[key] = words
+        yield wait("accum", 0, 0)
+        assert all(mma_done)
+
+    def issuer(r):
+        k0, step = (r, 2) if split else (0, 1)
+        for kt in range(k0, words, step):
+            yield wait(f"afull{kt % AB}", (kt // AB) & 1, kt // AB)
+            mma_q[r].append(kt)
+        mma_q[r].append("accum")
+
+    actors = [producer("X"), producer("V"), mask_producer()]
+    actors += [densify(g, wi) for g in range(dg) for wi in range(wpg)]
+    actors += [issuer(r) for r in range(issuers)]
+    pending = [next(a, None) for a in actors]
+
+    def can_run(req):
+        if req[0] == "step":
+            return True
+        _, bar, parity, _ = req
+        return (bars[bar].completed & 1) != parity
+
+    while True:
+        moves = [("actor", i) for i, req in enumerate(pending) if req is not None and can_run(req)]
+        moves += [("event", i) for i in range(len(events))]
+        moves += [("mma", r) for r in range(issuers) if mma_q[r]]
+        if not moves:
+            assert all(req is None for req in pending) and not events, "deadlock"
+            break
+        kind, i = moves[rng.integers(len(moves))]
+        if kind == "actor":
+            req = pending[i]
+            if req[0] == "wait":
+                _, bar, _, phase = req
+                assert bars[bar].completed > phase, (
+                    f"a parity wait on {bar} passed before its phase {phase} completed")
+            pending[i] = next(actors[i], None)
+        elif kind == "event":
+            what, idx = events.pop(i)
+            if what == "M":
+                sl = idx % slots
+                if idx >= slots:
+                    old = idx - slots
+                    assert all(dens_next[k] >= MWn * (old + 1) for k in dens_next), (
+                        f"mask box {idx} overwrote box {old} before its last reader")
+                mslot[sl] = idx
+                bars[f"mfull{sl}"].land()
+            else:
+                st = idx % S
+                assert idx < S or mma_done[idx - S], (
+                    f"stage {idx} overwrote slot {st} before the MMAs of stage {idx - S}")
+                (xslot if what == "X" else vslot)[st] = idx
+                bars[f"full{idx % FB}"].land()
         else:
-            i = m[1]
-            mma_done[mma_next[i]] = True
-            mma_next[i] += issuers if split else 1
-    assert released == [nwarps] * nbox
+            item = mma_q[i].pop(0)
+            if item == "accum":
+                bars["accum"].arrive()
+                continue
+            st = item % S
+            assert xslot[st] == item and all(a == item for a in aslot[st]), (
+                f"MMA of stage {item} read tiles of stages {xslot[st]} / {aslot[st]}")
+            mma_done[item] = True
+            if commit_last or item + S < words:
+                bars[f"empty{st}"].arrive()
+    assert all(mma_done)
 
 
 @pytest.mark.parametrize("vi", range(len(VARIANTS)))
-def test_mask_slots_are_not_refilled_before_their_last_reader(vi):
-    """Every densify group touches every box (DG <= MW) and releases it once
-    per warp; the mask producer's wait on the release barrier then keeps each
-    slot until its last reader is done, whatever the order the two K-split
-    issuers and the groups run in, and the pipeline always completes."""
+def test_barrier_protocol_under_any_completion_order(vi):
+    """Every variant's barrier protocol, including the K-split issuers and the
+    densify groups whose stage ring length is not a multiple of the group
+    count, stays exact under random completion orders of every copy and MMA:
+    each parity wait sees the phase it means, each reader its own stage, and
+    the block always completes."""
     _, _, stages = VARIANTS[vi]
     dg, split = DENSIFY_GROUPS[vi], MMA_SPLIT[vi]
     assert dg <= MW
-    rng = np.random.default_rng(1234 + vi)
-    for words in (MW, 2 * MW, 4 * MW, 64, 256):
-        for _ in range(6):
-            _run_pipeline(stages, dg, split, words, rng)
+    rng = np.random.default_rng(4321 + vi)
+    for words in (MW, 2 * MW, 3 * MW, 4 * MW, 9 * MW, 16 * MW):
+        for _ in range(24):
+            _run_block(stages, dg, split, words, rng)
 
 
 @pytest.mark.parametrize("mt", [True, False])
