@@ -588,27 +588,34 @@ size_t spmm_tc_workspace_bytes(int64_t rows, int words, int64_t T, int splits) {
 
 // Time model of a plan (variant, K slices), in ns: waves of blocks x (the
 // slice's stages x the variant's time per 32-column stage + a block's fixed
-// cost), plus, when split, the combine (a launch and its traffic).  Times per
-// stage measured on GB300 over the decoder-layer shapes, one block per SM:
-// 512 tokens 441 (5 stages), 256 tokens 319 (7), 128 tokens 232 (10), 64
-// tokens 218 (12).  A larger token tile does more work per stage; a smaller
-// one, or a K split, fills more SMs when rows (or tokens) are few.
+// cost + its output stores: fp16 Y, or fp32 sums when split), plus, when
+// split, the combine (a launch and its traffic).  Times per stage measured on
+// GB300 over the decoder-layer shapes, one block per SM: 512 tokens 441 (5
+// stages), 256 tokens 319 (7), 128 tokens 232 (10), 64 tokens 218 (12).  The
+// other constants were fitted to a sweep of every (variant, 1..8 slices) over
+// eight decoder matrices (4096..57344 rows, 4096..28672 columns) at 16, 64,
+// 256, 512 and 2048 tokens, on which the model picks the fastest plan in
+// every case.  A larger token tile does more work per stage; a smaller one,
+// or a K split, fills more SMs when rows (or tokens) are few.
 namespace {
 struct Cand {
   int variant, tokens;
   double ns_per_stage;
 };
 constexpr Cand kCand[] = {{4, 512, 441.0}, {1, 256, 319.0}, {2, 128, 232.0}, {3, 64, 218.0}};
-constexpr double kBlockNs = 3000.0;        // prologue, pipeline fill, epilogue
+constexpr double kBlockNs = 2000.0;        // prologue, pipeline fill, teardown
+constexpr double kStoreBytesPerNs = 40.0;  // one block's output stores (per SM)
 constexpr double kCombineNs = 2500.0;      // the combine kernel's launch and ramp
-constexpr double kCombineBytesPerNs = 5000.0;
+constexpr double kCombineBytesPerNs = 2000.0;  // partial sums written, read; Y written
 constexpr size_t kMaxSplitBytes = (size_t)256 << 20;
 
 double plan_ns(const Cand& c, int64_t rows, int words, int64_t T, int sms, int splits) {
   const int64_t tiles = ((rows + 127) / 128) * ((T + c.tokens - 1) / c.tokens);
   const int z = spmm_tc_slices(words, splits);
   const int64_t waves = (tiles * z + sms - 1) / sms;
-  double t = (double)waves * (spmm_tc_slice_words(words, splits) * c.ns_per_stage + kBlockNs);
+  const double out_bytes = (double)c.tokens * 128.0 * (z > 1 ? 4.0 : 2.0);
+  double t = (double)waves * (spmm_tc_slice_words(words, splits) * c.ns_per_stage + kBlockNs +
+                              out_bytes / kStoreBytesPerNs);
   if (z > 1)
     t += kCombineNs + (double)(4 * z + 4 * z + 2) * (double)T * (double)rows / kCombineBytesPerNs;
   return t;
