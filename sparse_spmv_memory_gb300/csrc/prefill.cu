@@ -530,26 +530,59 @@ static cudaError_t launch_tc_mt(const SpmmTcParams& p, cudaStream_t stream) {
 }
 
 // Y[t][r] = fp16(sum over slices z, in increasing z, of part[z][t][r]): the
-// K split's fixed-order combine (one rounding, no atomics).
+// K split's fixed-order combine (one rounding, no atomics).  V = 4: each
+// thread takes four consecutive rows (16-byte loads, one 8-byte store), and
+// issues the slices' loads four at a time; the additions keep slice order.
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+template <int V>
 __global__ void __launch_bounds__(256) splitk_sum_kernel(const float* __restrict__ part,
                                                          int slices, int64_t T, int64_t rows,
                                                          __half* __restrict__ Y, int64_t ldy) {
   const int64_t plane = T * rows;
   for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
-         r += (int64_t)gridDim.x * blockDim.x) {
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * V; r < rows;
+         r += (int64_t)gridDim.x * blockDim.x * V) {
       const float* q = part + t * rows + r;
-      float acc = q[0];
-      for (int z = 1; z < slices; ++z) acc += q[z * plane];
-      Y[t * ldy + r] = __float2half_rn(acc);
+      if (V == 4) {
+        float4 acc = *reinterpret_cast<const float4*>(q);
+        int z = 1;
+        for (; z + 3 < slices; z += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(q + z * plane);
+          const float4 b = *reinterpret_cast<const float4*>(q + (z + 1) * plane);
+          const float4 c = *reinterpret_cast<const float4*>(q + (z + 2) * plane);
+          const float4 d = *reinterpret_cast<const float4*>(q + (z + 3) * plane);
+          acc = add4(add4(add4(add4(acc, a), b), c), d);
+        }
+        for (; z < slices; ++z) acc = add4(acc, *reinterpret_cast<const float4*>(q + z * plane));
+        const __half2 lo = __floats2half2_rn(acc.x, acc.y), hi = __floats2half2_rn(acc.z, acc.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(Y + t * ldy + r) = w;
+      } else {
+        float acc = q[0];
+        for (int z = 1; z < slices; ++z) acc += q[z * plane];
+        Y[t * ldy + r] = __float2half_rn(acc);
+      }
     }
   }
 }
 
 static cudaError_t launch_splitk_sum(const SpmmTcParams& p, cudaStream_t stream) {
-  const int64_t bx = (p.rows + 255) / 256;
+  // Four rows a thread when every row group of Y is 8-byte aligned (the
+  // partial planes then are 16-byte aligned: the workspace is).
+  const bool v4 = p.rows % 4 == 0 && p.ldy % 4 == 0 &&
+                  (reinterpret_cast<uintptr_t>(p.Y) & 7) == 0;
+  const int64_t per_block = v4 ? 1024 : 256;
+  const int64_t bx = (p.rows + per_block - 1) / per_block;
   const dim3 grid((unsigned)(bx < 65535 ? bx : 65535), (unsigned)(p.T < 65535 ? p.T : 65535));
-  splitk_sum_kernel<<<grid, 256, 0, stream>>>(p.part, p.slices, p.T, p.rows, p.Y, p.ldy);
+  if (v4)
+    splitk_sum_kernel<4><<<grid, 256, 0, stream>>>(p.part, p.slices, p.T, p.rows, p.Y, p.ldy);
+  else
+    splitk_sum_kernel<1><<<grid, 256, 0, stream>>>(p.part, p.slices, p.T, p.rows, p.Y, p.ldy);
   return cudaGetLastError();
 }
 
@@ -603,10 +636,10 @@ struct Cand {
   double ns_per_stage;
 };
 constexpr Cand kCand[] = {{4, 512, 441.0}, {1, 256, 319.0}, {2, 128, 232.0}, {3, 64, 218.0}};
-constexpr double kBlockNs = 2000.0;        // prologue, pipeline fill, teardown
-constexpr double kStoreBytesPerNs = 40.0;  // one block's output stores (per SM)
+constexpr double kBlockNs = 3000.0;        // prologue, pipeline fill, teardown
+constexpr double kStoreBytesPerNs = 80.0;  // one block's output stores (per SM)
 constexpr double kCombineNs = 2500.0;      // the combine kernel's launch and ramp
-constexpr double kCombineBytesPerNs = 2000.0;  // partial sums written, read; Y written
+constexpr double kCombineBytesPerNs = 8000.0;  // partial sums written, read; Y written
 constexpr size_t kMaxSplitBytes = (size_t)256 << 20;
 
 double plan_ns(const Cand& c, int64_t rows, int words, int64_t T, int sms, int splits) {
