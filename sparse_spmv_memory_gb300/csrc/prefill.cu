@@ -12,26 +12,31 @@
 //  * A block owns a tile of BM = 128 rows of W and BN = NB * NMMA tokens; its
 //    fp32 accumulator D (128 x BN) lives in tensor memory, row m in TMEM lane
 //    m.  K advances one mask word (32 columns) per pipeline stage.
-//  * Two producer warps, each a short chain of asynchronous copies per stage
-//    so that the two run side by side: warp 0 loads the token tile of X by
-//    TMA (BN x 32 fp16, 64-byte swizzle); warp 2 loads the tile's compact
-//    values (128 rows x 16 fp16) by TMA and its mask words (by TMA, four
-//    stages per box on a barrier of the box's own, when the mask pitch allows
-//    it, else by cp.async).  Values and X complete on the stage's "full"
-//    mbarrier.
+//  * Producer warps, each a short chain of asynchronous copies per stage so
+//    that they run side by side: warp 0 loads the token tile of X by TMA
+//    (BN x 32 fp16, 64-byte swizzle); warp 2 loads the tile's compact values
+//    (128 rows x 16 fp16) by TMA; the mask words come by TMA from a warp of
+//    their own, four stages per box on a barrier of the box's own, when the
+//    mask pitch allows it, else by cp.async from warp 2.  Values and X
+//    complete on the stage's "full" mbarrier.
 //  * Warps 3..18 (densify), in DG groups that take alternate stages: expand
 //    each row's 16 kept values into the 32 columns of a K-major,
 //    64-byte-swizzled fp16 tile in shared memory, the layout the MMA
-//    descriptor names.  A lane builds two adjacent columns: the rank of its
-//    first column among the word's set bits (one popc) indexes its value in
-//    the compact row; one table-driven prmt places it, its neighbour or zeros.
-//  * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (M = 128,
-//    N = NMMA, K = 16; two per stage and N-part) on the densified tile and the
-//    X tile, and tcgen05.commit frees the stage when those MMAs are done.
+//    descriptor names.  A lane builds four adjacent columns as two pairs:
+//    the rank of a pair's first column among the word's set bits (popc)
+//    indexes its value in the compact row; one table-driven prmt places it,
+//    its neighbour or zeros.
+//  * MMA: one thread (warp 1), or two taking the even and odd stages into two
+//    accumulators, issues tcgen05.mma kind::f16 (M = 128, N = NMMA, K = 16;
+//    two per stage and N-part) on the densified tile and the X tile, and
+//    tcgen05.commit frees the stage when those MMAs are done.
 //  * Epilogue (warps 3..18): tcgen05.ld of the accumulator, fp32 -> fp16 RNE,
-//    stores to Y[t][r].
-//  * Every mbarrier wait gives up after kWaitLimitNs (counted in
-//    g_wait_timeouts); the roles then skip to teardown, which waits for the
+//    stores to Y[t][r]; or, under a K split across blocks (grid z: each block
+//    one slice of the row's mask words), fp32 stores of the slice's sums, which
+//    splitk_sum_kernel adds in slice order.
+//  * The stage barriers are rings sized so that every parity wait is exact
+//    (see Layout).  Every mbarrier wait gives up after kWaitLimitNs (counted
+//    in g_wait_timeouts); the roles then skip to teardown, which waits for the
 //    copies and MMAs already issued before tensor memory is freed.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -57,7 +62,7 @@ constexpr int MT_SLOT = BM * MW * 4;   // 2 KiB: the masks of MW consecutive sta
 // Densify warps per block (DW, a kernel parameter) follow the producer and
 // MMA warps.  16 measured best on GB300: 8 left the per-stage chains
 // exposed, 24 lost to the extra shared-memory and issue contention.
-// After them: a second MMA issuer (used by the K-split variants) and the
+// After them: a second MMA issuer (used by the two-issuer variants) and the
 // producer of the mask boxes.
 constexpr int FIRST_DENSIFY_WARP = 3;
 __host__ __device__ constexpr int mma2_warp(int dw) { return FIRST_DENSIFY_WARP + dw; }
@@ -75,7 +80,7 @@ constexpr uint32_t tmem_cols_for(int n) {
 // MW * MT_SLOTS >= STAGES + MW - 1 boxes in flight keep the box of every
 // stage in the pipeline resident while the densify warps reach it.
 // MS: 0, one thread issues every stage's MMAs; 1, two threads take the even
-// and odd stages into two accumulators that the epilogue adds (K split).
+// and odd stages into two accumulators that the epilogue adds.
 constexpr int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
 
 template <int NMMA, int NB, int STAGES, int DG, int MS, bool MT>
@@ -106,7 +111,7 @@ struct Layout {
   static constexpr int BYTES = SLOT_OFF + 16;
   static constexpr int SMEM = BYTES + 1024;  // room to align the base to 1024
   static constexpr uint32_t TMEM_COLS = tmem_cols_for(MS ? 2 * BN : BN);
-  static_assert(!MS || 2 * BN <= 512, "the K split keeps two accumulators in tensor memory");
+  static_assert(!MS || 2 * BN <= 512, "two issuers keep two accumulators in tensor memory");
   static_assert(!MT || MW * MT_SLOTS >= STAGES + MW - 1, "mask slot reused too early");
   static_assert(NMMA % 16 == 0 && NMMA >= 16 && NMMA <= 256, "tcgen05 M=128 needs N in 16..256");
   static_assert(BN >= 64 && BN <= 512 && BN % 32 == 0, "epilogue reads 32-column chunks");
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
                    int wslice, int64_t T, int64_t ldy, uint64_t wait_limit_ns, int stall_weights) {
   using L = Layout<NMMA, NB, STAGES, DG, MS, MT>;
   static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
-  static_assert(MS == 0 || G == 1, "each K-split issuer waits on each of its stages");
+  static_assert(MS == 0 || G == 1, "each of two issuers waits on each of its stages");
   static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
   static_assert(threads_for(DW) <= 1024, "a block has at most 1024 threads");
   static_assert(DG <= MW, "every densify group must read every mask box, in order");

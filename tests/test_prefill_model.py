@@ -241,7 +241,7 @@ def _run_block(stages, dg, split, words, rng, wpg=2, rings=True, commit_last=Fal
     producer and a W producer (stage kt after the MMAs of stage kt - STAGES
     released its slot), the mask producer (box b after every densify warp
     released box b - slots), DG groups of densify warps (group g takes stages
-    g, g + DG, ...), one or two MMA issuers (with the K split: even / odd
+    g, g + DG, ...), one or two MMA issuers (two: even / odd
     stages), and the copies and MMAs as asynchronous events that complete in
     any order (the MMAs of one issuer in issue order).  Actors and events run
     in random order with real parity-wait semantics.  Checks: every wait
@@ -382,7 +382,7 @@ def _run_block(stages, dg, split, words, rng, wpg=2, rings=True, commit_last=Fal
 
 @pytest.mark.parametrize("vi", range(len(VARIANTS)))
 def test_barrier_protocol_under_any_completion_order(vi):
-    """Every variant's barrier protocol, including the K-split issuers and the
+    """Every variant's barrier protocol, including the two-issuer variants and the
     densify groups whose stage ring length is not a multiple of the group
     count, stays exact under random completion orders of every copy and MMA:
     each parity wait sees the phase it means, each reader its own stage, and
