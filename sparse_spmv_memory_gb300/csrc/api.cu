@@ -507,6 +507,22 @@ size_t nm_spmm_prefill_workspace_bytes(int64_t rows, int64_t cols, int64_t T) {
   return nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, -1, 0);
 }
 
+int nm_spmm_prefill_plan(int64_t rows, int64_t cols, int64_t T, int sms, int* variant,
+                         int* slices) {
+  if (!prefill_shape_ok(rows, cols, T) || rows == 0 || T == 0) return NM_ERR_SHAPE;
+  if (sms <= 0) {
+    DeviceInfo d;
+    if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+    sms = d.sms;
+  }
+  const int words = (int)(cols / 32);
+  int v, z;
+  spmm_tc_default_plan(rows, words, T, sms, -1, 0, kPrefillMaxSplits, &v, &z);
+  if (variant) *variant = v;
+  if (slices) *slices = spmm_tc_slices(words, z);
+  return NM_OK;
+}
+
 int nm_spmm_prefill_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                        const void* X, int64_t ldx, int64_t T, void* Y, int64_t ldy, int variant,
                        int splits, void* workspace, size_t workspace_bytes, void* stream) {

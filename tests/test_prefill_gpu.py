@@ -308,6 +308,29 @@ def test_nm_spmm_beyond_eight_tokens_takes_the_tensor_core_path(nm, orc):
     assert np.all(np.abs(f16_to_f64(a) - y_ref) <= oracle.tolerance(s))
 
 
+def test_nm_spmm_beyond_eight_tokens_asks_for_the_split_workspace(nm):
+    """nm_spmm's workspace query covers the tensor-core plan beyond 8 tokens:
+    a shape whose plan splits needs that workspace, and is refused without."""
+    L = nm.lib()
+    rows, cols, T = 1024, 8192, 64
+    need = L.nm_spmm_workspace_bytes(rows, cols, T)
+    assert need == nm.nm_spmm_prefill_workspace_bytes(rows, cols, T) > 0
+    v = torch.zeros(rows * cols // 2, dtype=torch.float16, device="cuda")
+    m = torch.zeros(rows * cols // 32, dtype=torch.int32, device="cuda")
+    X = torch.zeros((T, cols), dtype=torch.float16, device="cuda")
+    Y = torch.zeros((T, rows), dtype=torch.float16, device="cuda")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()
+    args = (P(v), P(m), rows, cols, P(X), cols, T, P(Y), rows)
+    assert L.nm_spmm(*args, None, 0, st) == 5
+    assert L.nm_spmm(*args, P(ws), need - 16, st) == 5
+    assert L.nm_spmm(*args, P(ws), need, st) == 0
+    torch.cuda.synchronize()
+    assert bool((Y == 0).all())     # all-zero weights: zero output
+    assert nm.nm_wait_timeouts() == 0
+
+
 def test_bounded_waits_end_a_stalled_prefill_kernel(nm, orc):
     """Self-test of the failure path: with its weight producer disabled no
     stage ever completes; every wait runs out after the given limit, is
