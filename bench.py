@@ -731,6 +731,7 @@ def run_prefill(args):
     ws_bytes = [nm.nm_spmm_prefill_workspace_bytes(r, c, T) for _, r, c in mats]
     ws = [torch.empty(b, dtype=torch.uint8, device=device) if b else None for b in ws_bytes]
     k_slices = {n: (b // (4 * T * r) if b else 1) for (n, r, _), b in zip(mats, ws_bytes)}
+    tile_tokens = {n: nm.nm_spmm_prefill_plan(r, c, T)[2] for n, r, c in mats}
 
     def run_sparse():
         for l in range(layers):
@@ -814,7 +815,7 @@ def run_prefill(args):
                           f"{sum(sparse_bytes(r, c) for _, r, c in mats) / 1e9:.2f} GB each "
                           "(129 MB L2) cycled over the layers"),
             "parallelism": f"replicas x{world}", "kernel_variant": "library default for T",
-            "k_slices": k_slices,
+            "k_slices": k_slices, "tile_tokens": tile_tokens,
         },
         "gpu_launches": layers * k * sum(1 if z == 1 else 2 for z in k_slices.values()),
         "us_per_call": per_matrix,

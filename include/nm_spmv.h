@@ -301,10 +301,11 @@ int nm_spmm_prefill_ex(const void *values, const uint32_t *masks, int64_t rows, 
 int nm_spmm_prefill_variant_count(void);
 /* nm_spmm_prefill_plan -- the plan nm_spmm_prefill_ws takes for this shape on
  * a device with `sms` SMs (<= 0: the current device's count): the kernel
- * variant and the number of K slices (1: no split).  Host-only when sms > 0.
+ * variant, the number of K slices (1: no split) and the tokens per block of
+ * that variant.  Any output pointer may be NULL.  Host-only when sms > 0.
  * rows, T >= 1 and cols % 32 == 0, else NM_ERR_SHAPE. */
 int nm_spmm_prefill_plan(int64_t rows, int64_t cols, int64_t T, int sms, int *variant,
-                         int *slices);
+                         int *slices, int *tile_tokens);
 
 /* nm_wait_timeouts -- how many times a tensor-core kernel's bounded wait on
  * one of its own barriers gave up (each such wait ends after 2 s, after which

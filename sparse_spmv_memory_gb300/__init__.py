@@ -96,7 +96,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_spmm_prefill_ws": ([P, P, I64, I64, P, I64, I64, P, I64, P, SZ, P], I32),
         "nm_spmm_prefill_workspace_bytes": ([I64, I64, I64], SZ),
         "nm_spmm_prefill_workspace_bytes_ex": ([I64, I64, I64, I32, I32], SZ),
-        "nm_spmm_prefill_plan": ([I64, I64, I64, I32, P, P], I32),
+        "nm_spmm_prefill_plan": ([I64, I64, I64, I32, P, P, P], I32),
         "nm_spmm_prefill_variant_count": ([], I32),
         "nm_wait_timeouts": ([I32], I64),
         "nm_prefill_stall_selftest": ([P, P, I64, I64, P, I64, I64, P, I64, I64, P], I32),
@@ -317,13 +317,13 @@ def nm_spmm_prefill_workspace_bytes(rows: int, cols: int, T: int, variant: int =
     return L.nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, variant, splits)
 
 
-def nm_spmm_prefill_plan(rows: int, cols: int, T: int, sms: int = 0) -> tuple[int, int]:
-    """(kernel variant, K slices) nm_spmm_prefill_ws takes for this shape on a
-    device with ``sms`` SMs (0: the current device)."""
-    v, z = ctypes.c_int(), ctypes.c_int()
-    _check(lib().nm_spmm_prefill_plan(rows, cols, T, sms, ctypes.byref(v), ctypes.byref(z)),
-           "nm_spmm_prefill_plan")
-    return v.value, z.value
+def nm_spmm_prefill_plan(rows: int, cols: int, T: int, sms: int = 0) -> tuple[int, int, int]:
+    """(kernel variant, K slices, tokens per block) nm_spmm_prefill_ws takes for
+    this shape on a device with ``sms`` SMs (0: the current device)."""
+    v, z, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().nm_spmm_prefill_plan(rows, cols, T, sms, ctypes.byref(v), ctypes.byref(z),
+                                      ctypes.byref(n)), "nm_spmm_prefill_plan")
+    return v.value, z.value, n.value
 
 
 def nm_spmm_prefill(values, masks, X, Y=None, workspace=None, stream=None, variant: int = -1,

@@ -508,7 +508,7 @@ size_t nm_spmm_prefill_workspace_bytes(int64_t rows, int64_t cols, int64_t T) {
 }
 
 int nm_spmm_prefill_plan(int64_t rows, int64_t cols, int64_t T, int sms, int* variant,
-                         int* slices) {
+                         int* slices, int* tile_tokens) {
   if (!prefill_shape_ok(rows, cols, T) || rows == 0 || T == 0) return NM_ERR_SHAPE;
   if (sms <= 0) {
     DeviceInfo d;
@@ -520,6 +520,7 @@ int nm_spmm_prefill_plan(int64_t rows, int64_t cols, int64_t T, int sms, int* va
   spmm_tc_default_plan(rows, words, T, sms, -1, 0, kPrefillMaxSplits, &v, &z);
   if (variant) *variant = v;
   if (slices) *slices = spmm_tc_slices(words, z);
+  if (tile_tokens) *tile_tokens = spmm_tc_block_tokens(v);
   return NM_OK;
 }
 

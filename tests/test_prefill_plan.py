@@ -38,8 +38,9 @@ def test_plan_is_whole_boxes_and_matches_the_workspace(nm):
         cols = 32 * int(rng.integers(1, 1000))
         T = int(rng.integers(1, 4096))
         sms = int(rng.choice([1, 8, 76, 132, 152, 304]))
-        v, z = nm.nm_spmm_prefill_plan(rows, cols, T, sms)
+        v, z, tokens = nm.nm_spmm_prefill_plan(rows, cols, T, sms)
         assert 0 <= v < nm.nm_spmm_prefill_variant_count()
+        assert tokens in (64, 128, 256, 512)
         assert 1 <= z <= 8
         assert slices_of(cols // 32, z) == z
         ws = nm.nm_spmm_prefill_workspace_bytes(rows, cols, T, v, z)
@@ -63,7 +64,7 @@ def test_few_row_tiles_split_and_long_prompts_do_not(nm):
     assert plans[(57344, 8192, 64)][1] == 1
     # 2048 tokens: four 512-token tiles per row tile, no split, largest token tile
     for r, c in LAYER_70B:
-        assert plans[(r, c, 2048)] == (4, 1), (r, c)
+        assert plans[(r, c, 2048)] == (4, 1, 512), (r, c)
     assert nm.nm_spmm_prefill_plan(1024, 8192, 64, GB300_SMS)[1] > 1
 
 
@@ -72,4 +73,5 @@ def test_plan_refuses_bad_shapes(nm):
     L = nm.lib()
     v, z = ctypes.c_int(), ctypes.c_int()
     for rows, cols, T in [(0, 64, 8), (64, 48, 8), (64, 64, 0), (-1, 64, 8)]:
-        assert L.nm_spmm_prefill_plan(rows, cols, T, 152, ctypes.byref(v), ctypes.byref(z)) == 2
+        assert L.nm_spmm_prefill_plan(rows, cols, T, 152, ctypes.byref(v), ctypes.byref(z),
+                                      None) == 2
