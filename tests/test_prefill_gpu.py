@@ -271,6 +271,39 @@ def test_prefill_many_short_blocks_repeatable(nm, orc):
         assert np.all(np.abs(f16_to_f64(Yh[t, row_ids]) - y_ref) <= oracle.tolerance(s))
 
 
+def test_prefill_every_plan_agrees_on_random_shapes(nm):
+    """Seeded random shapes (both mask paths, all four patterns, ragged tiles)
+    on exact-arithmetic inputs: every variant at 1, 2, 3, 5 and 8 K slices
+    gives the same bits as the unsplit 64-token variant (itself checked
+    against the oracle above), and no bounded wait runs out.  A soak of the
+    barrier protocol under many short blocks and pipeline depths."""
+    rng = np.random.default_rng(96)
+    nm.nm_wait_timeouts(reset=True)
+    done = 0
+    while done < 400:
+        rows = int(rng.integers(1, 1500))
+        words = int(rng.integers(1, 96))
+        T = int(rng.integers(1, 600))
+        cols = 32 * words
+        if rows * cols * T > 4e8:
+            continue
+        N, M = PATTERNS[done % 4]
+        W = synth.int_f16((rows, cols), 0, synth.stream_id(96, done, 0), -8, 8, -6)
+        X = synth.int_f16((T, cols), 0, synth.stream_id(96, done, 1), -2, 2, 0)
+        Wd = to_dev(W)
+        v, m = nm.nm_pack(Wd, N, M)
+        del Wd
+        Xd = to_dev(X)
+        ref = nm.nm_spmm_prefill(v, m, Xd, variant=3, splits=1)
+        for variant in range(nm.nm_spmm_prefill_variant_count()):
+            for splits in (1, 2, 3, 5, 8):
+                Y = nm.nm_spmm_prefill(v, m, Xd, variant=variant, splits=splits)
+                assert torch.equal(Y.view(torch.int16), ref.view(torch.int16)), (
+                    rows, cols, T, (N, M), variant, splits)
+        done += 1
+    assert nm.nm_wait_timeouts() == 0
+
+
 def test_prefill_nonfinite_activation_is_dense_semantics(nm, orc):
     """Pruned weights enter the MMA as +0: an infinite X[t][c] makes every row
     that prunes column c NaN (0 * inf) and every row that keeps it +-inf (the
