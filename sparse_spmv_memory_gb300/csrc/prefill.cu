@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
                    int wslice, int64_t T, int64_t ldy, uint64_t wait_limit_ns, int stall_weights) {
   using L = Layout<NMMA, NB, STAGES, DG, MS, MT>;
   static_assert(DG == 1 || G == 1, "waiting on every second stage needs one densify group");
+  // G = 2 waits on the odd stages' afull barriers only; with an even ring each
+  // of those barriers serves odd stages alone, so every parity wait stays exact.
+  static_assert(G == 1 || L::AFULL_RING % 2 == 0, "waiting on every second stage needs an even ring");
   static_assert(MS == 0 || G == 1, "each of two issuers waits on each of its stages");
   static_assert(DW % DG == 0 && DW % 4 == 0, "equal densify groups, whole TMEM quadrants");
   static_assert(threads_for(DW) <= 1024, "a block has at most 1024 threads");
