@@ -413,6 +413,27 @@ def test_layout_fits_and_is_aligned(nmma, nb, stages, mt):
     assert L["BN"] % 32 == 0
 
 
+def test_model_variants_match_the_kernel_table():
+    """The variants this model checks are the kernel's: (tokens per MMA, MMAs
+    per stage, stages, densify groups, two issuers) parsed from the table in
+    prefill.cu, so a change there cannot leave the model checking another
+    protocol."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "sparse_spmv_memory_gb300", "csrc", "prefill.cu")).read()
+    table = re.search(r"kVariants\[\]\s*=\s*\{(.*?)\};", src, re.S).group(1)
+    rows = [tuple(int(x) for x in t.split(",")) for t in re.findall(r"\{([^{}]*)\}", table)]
+    assert [(r[0], r[1], r[2]) for r in rows] == VARIANTS
+    assert [r[4] for r in rows] == DENSIFY_GROUPS
+    assert [r[6] for r in rows] == MMA_SPLIT
+    assert all(r[3] == 1 and r[5] == DENSIFY_WARPS for r in rows)
+    # the launch switch instantiates exactly these variants, case i = row i
+    cases = re.findall(r"case (\d+): return tc::launch_tc<([^>]*)>", src)
+    assert [int(i) for i, _ in cases] == list(range(len(rows)))
+    assert [tuple(int(x) for x in a.split(",")) for _, a in cases] == rows
+
+
 def test_instruction_and_smem_descriptors():
     """Bit positions of the kind::f16 instruction descriptor and the 64-byte
     swizzled K-major shared-memory descriptor the kernel builds."""
