@@ -432,6 +432,10 @@ def test_model_variants_match_the_kernel_table():
     cases = re.findall(r"case (\d+): return tc::launch_tc<([^>]*)>", src)
     assert [int(i) for i, _ in cases] == list(range(len(rows)))
     assert [tuple(int(x) for x in a.split(",")) for _, a in cases] == rows
+    # the plan's candidates name each variant with its own tile
+    cand = re.search(r"kCand\[\]\s*=\s*\{(.*?)\};", src, re.S).group(1)
+    for v, tokens in re.findall(r"\{(\d+),\s*(\d+),", cand):
+        assert rows[int(v)][0] * rows[int(v)][1] == int(tokens), (v, tokens)
 
 
 def test_instruction_and_smem_descriptors():
