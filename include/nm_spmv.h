@@ -284,8 +284,10 @@ int64_t nm_check_masks(const uint32_t *masks, int64_t rows, int64_t cols, void *
  * multiples of four, so fewer may result); the workspace it needs is
  * nm_spmm_prefill_workspace_bytes_ex(rows, cols, T, variant, splits).  The
  * chosen plan minimises a time model: waves of blocks x (a slice's stages x
- * each variant's measured time per stage + a block's fixed cost), plus the
- * combine's launch and traffic when split.
+ * each variant's measured time per stage + a block's fixed cost + its output
+ * stores), plus the combine's launch and traffic when split; it considers at
+ * most 8 slices and at most 256 MB of partial sums.  nm_spmm_prefill_plan
+ * reports it.
  * ------------------------------------------------------------------------- */
 int nm_spmm_prefill(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
                     const void *X, int64_t ldx, int64_t T, void *Y, int64_t ldy, void *stream);
