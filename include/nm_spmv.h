@@ -337,9 +337,13 @@ int nm_prefill_stall_selftest(const void *values, const uint32_t *masks, int64_t
  *   Scratch: a fixed array inside the library's device image (32 KB + 8 B),
  *   held by every GPU that loads the library until the process exits.
  *   Limit: rows * cols / 32 <= NM_CHECK_NOALLOC_MAX_WORDS mask words;
- *   larger inputs return -NM_ERR_WORKSPACE without launching anything.
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   larger inputs (including any whose product would overflow) return
+ *   -NM_ERR_WORKSPACE without any CUDA call.
+ *   The first call in a CUDA context looks up the array's device address in
+ *   that context (cudaGetSymbolAddress, which also loads the module) and
+ *   caches it under the context's unique id, so a context made after
+ *   cudaDeviceReset gets a fresh lookup; make that first call before any
+ *   stream capture.
  *   All calls share the array: calls that overlap on the GPU (different
  *   streams or host threads at the same time) race and must be serialised by
  *   the caller.  Each call writes every scratch slot it reads, so nothing

@@ -63,6 +63,7 @@ using namespace nmk;
 namespace {
 
 constexpr int64_t kMaxRows = (int64_t)1 << 31;
+constexpr int64_t kMaxCols = (int64_t)1 << 31;  // words per row then fit an int
 constexpr int kPrefillMaxSplits = 8;   // K slices the prefill plan considers
 constexpr int kPrefillMaxSlices = 64;  // K slices a caller may ask for
 
@@ -187,7 +188,8 @@ size_t spmm_workspace_for(const SpmmParams& p) {
 int check_spmv_args(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                     const void* x, const void* y) {
   if (!values || !masks || !x || !y) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return NM_ERR_SHAPE;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0) return NM_ERR_SHAPE;
   if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(x, 16) || !aligned(y, 2))
     return NM_ERR_ALIGN;
   const size_t yb = (size_t)rows * 2;
@@ -236,7 +238,7 @@ size_t nm_masks_bytes(int64_t rows, int64_t cols) {
 }
 
 size_t nm_spmv_workspace_bytes(int64_t rows, int64_t cols) {
-  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return 0;
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols || cols % 32 != 0) return 0;
   const int64_t max_cols = nm_spmv_max_cols();
   if (max_cols < 0 || cols <= max_cols) return 0;  // the whole row's x tile fits
   // longer rows run as a one-token nm_spmm over column slices
@@ -260,7 +262,8 @@ int64_t nm_spmv_max_cols(void) {
 int nm_pack(const void* W, int64_t rows, int64_t cols, int64_t ld, int N, int M, void* values,
             uint32_t* masks, void* stream) {
   if (!W || !values || !masks) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
   if (!valid_pattern(N, M)) return NM_ERR_PATTERN;
   if (!aligned(W, 2) || !aligned(values, 16) || !aligned(masks, 4)) return NM_ERR_ALIGN;
   const size_t wb = (size_t)((rows - 1) * ld + cols) * 2;
@@ -277,7 +280,8 @@ int nm_pack(const void* W, int64_t rows, int64_t cols, int64_t ld, int N, int M,
 int nm_unpack(const void* values, const uint32_t* masks, int64_t rows, int64_t cols, void* W_out,
               int64_t ld, void* stream) {
   if (!values || !masks || !W_out) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0 || ld < cols) return NM_ERR_SHAPE;
   if (!aligned(values, 16) || !aligned(masks, 4) || !aligned(W_out, 2)) return NM_ERR_ALIGN;
   const size_t wb = (size_t)((rows - 1) * ld + cols) * 2;
   if (rows && (overlap(W_out, wb, values, (size_t)rows * cols) ||
@@ -320,7 +324,8 @@ int nm_spmv_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
 int nm_spmv_swiglu_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
                       const void* x, void* h, int variant, int grid, int flags, void* stream) {
   if (!values || !masks || !x || !h) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || rows % 2 != 0 || cols <= 0 || cols % 32 != 0)
+  if (rows < 0 || rows >= kMaxRows || rows % 2 != 0 || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0)
     return NM_ERR_SHAPE;
   if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(x, 16) || !aligned(h, 2))
     return NM_ERR_ALIGN;
@@ -361,7 +366,8 @@ int nm_spmv(const void* values, const uint32_t* masks, int64_t rows, int64_t col
 }
 
 int nm_spmv_plan(int64_t rows, int64_t cols, int* variant, int* grid, int* warps) {
-  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0) return NM_ERR_SHAPE;
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0) return NM_ERR_SHAPE;
   SpmvPlan plan;
   SpmvParams p;
   int st = make_spmv_plan(rows, cols, -1, 0, &plan, &p);
@@ -379,7 +385,8 @@ int dense_gemv_variant_count(void) { return gemv_variant_count(); }
 int dense_gemv_ex(const void* W, int64_t rows, int64_t cols, int64_t ld, const void* x, void* y,
                   int variant, int grid, int flags, void* stream) {
   if (!W || !x || !y) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 8 != 0 || ld < cols) return NM_ERR_SHAPE;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 8 != 0 || ld < cols) return NM_ERR_SHAPE;
   if (!aligned(W, 16) || ld % 8 != 0 || !aligned(x, 16) || !aligned(y, 2)) return NM_ERR_ALIGN;
   const size_t yb = (size_t)rows * 2;
   if (rows && (overlap(y, yb, W, (size_t)((rows - 1) * ld + cols) * 2) ||
@@ -406,7 +413,8 @@ int dense_gemv(const void* W, int64_t rows, int64_t cols, int64_t ld, const void
 
 size_t nm_spmm_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant,
                                   int slices) {
-  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || batch < 1 || batch > 8)
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0 || batch < 1 || batch > 8)
     return 0;
   SpmmPlan plan;
   SpmmParams p;
@@ -426,7 +434,8 @@ int nm_spmm_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t 
                size_t workspace_bytes, int variant, int grid, int slices, int flags,
                void* stream) {
   if (!values || !masks || !X || !Y) return NM_ERR_NULL;
-  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols % 32 != 0 || batch < 1 || batch > 8 ||
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols ||
+      cols % 32 != 0 || batch < 1 || batch > 8 ||
       ldx < cols || ldy < rows)
     return NM_ERR_SHAPE;
   if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
@@ -490,7 +499,7 @@ static int prefill_plan(int64_t rows, int64_t cols, int64_t T, int variant, int 
 
 static bool prefill_shape_ok(int64_t rows, int64_t cols, int64_t T) {
   return rows >= 0 && rows < kMaxRows && (rows + 127) / 128 <= 65535 && cols > 0 &&
-         cols % 32 == 0 && T >= 0 && T < kMaxRows;
+         cols < kMaxCols && cols % 32 == 0 && T >= 0 && T < kMaxRows;
 }
 
 size_t nm_spmm_prefill_workspace_bytes_ex(int64_t rows, int64_t cols, int64_t T, int variant,
@@ -584,9 +593,9 @@ int nm_prefill_stall_selftest(const void* values, const uint32_t* masks, int64_t
                               int64_t cols, const void* X, int64_t ldx, int64_t T, void* Y,
                               int64_t ldy, int64_t wait_limit_us, void* stream) {
   if (!values || !masks || !X || !Y) return NM_ERR_NULL;
-  if (rows <= 0 || rows >= kMaxRows || (rows + 127) / 128 > 65535 || cols <= 0 || cols % 32 != 0 ||
-      T <= 0 || T >= kMaxRows || ldx < cols || ldy < rows || wait_limit_us <= 0 ||
-      wait_limit_us > 2000000)
+  if (rows <= 0 || rows >= kMaxRows || (rows + 127) / 128 > 65535 || cols <= 0 ||
+      cols >= kMaxCols || cols % 32 != 0 || T <= 0 || T >= kMaxRows || ldx < cols ||
+      ldy < rows || wait_limit_us <= 0 || wait_limit_us > 2000000)
     return NM_ERR_SHAPE;
   if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
       !aligned(Y, 2))
@@ -614,7 +623,10 @@ int64_t nm_wait_timeouts(int reset) {
 
 int64_t nm_check_masks(const uint32_t* masks, int64_t rows, int64_t cols, void* stream) {
   if (!masks) return -NM_ERR_NULL;
-  if (rows < 0 || cols <= 0 || cols % 32 != 0) return -NM_ERR_SHAPE;
+  // the same row bound as the other entry points, and a column bound, so that
+  // rows * cols / 32 cannot wrap
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols || cols % 32 != 0)
+    return -NM_ERR_SHAPE;
   if (!aligned(masks, 4)) return -NM_ERR_ALIGN;
   if (rows == 0) return 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -19,7 +19,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "../../include/nm_spmv.h"
 
@@ -65,21 +65,72 @@ __global__ void sum_partials_kernel(unsigned long long* scratch, int blocks) {
   }
 }
 
-constexpr int kMaxDevices = 64;
-std::atomic<unsigned long long*> g_scratch_ptr[kMaxDevices];
+// The device address of g_check_scratch.  In host code the symbol's name is
+// only a host-side stand-in; the address belongs to the module loaded into a
+// CUDA context, so it is looked up (cudaGetSymbolAddress) once per context,
+// with that context current, and cached under the context's unique id.  A
+// context made after cudaDeviceReset, or a second driver-API context on the
+// same device, has a new id and gets its own lookup.  The lookup also loads
+// the module, which is why the first call in a context should come before any
+// stream capture.  If the driver entry points for the context id cannot be
+// had, the address is looked up on every call instead (a host-only query).
+using CtxGetCurrentFn = int (*)(void** ctx);
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
 
-// The device address of g_check_scratch on the current device, looked up once
-// per device (in host code the symbol's name is only a host-side stand-in).
-cudaError_t scratch_on_current_device(unsigned long long** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+struct CtxEntry {
+  unsigned long long id;
+  unsigned long long* ptr;
+};
+
+constexpr int kCachedContexts = 64;
+std::mutex g_scratch_mutex;
+CtxEntry g_scratch_cache[kCachedContexts];
+int g_scratch_cached = 0;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+bool g_driver_looked_up = false;
+
+// Unique id of the current context; false if there is none or it is unknown.
+bool current_context_id(unsigned long long* id) {
+  if (!g_driver_looked_up) {
+    g_driver_looked_up = true;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+      g_ctx_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+  }
+  if (!g_ctx_current || !g_ctx_id) return false;
+  void* ctx = nullptr;
+  if (g_ctx_current(&ctx) != 0 || ctx == nullptr) return false;
+  return g_ctx_id(ctx, id) == 0;
+}
+
+cudaError_t scratch_in_current_context(unsigned long long** out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  unsigned long long id = 0;
+  if (current_context_id(&id)) {
+    for (int i = 0; i < g_scratch_cached; ++i)
+      if (g_scratch_cache[i].id == id) {
+        *out = g_scratch_cache[i].ptr;
+        return cudaSuccess;
+      }
+  }
+  unsigned long long* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_check_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  unsigned long long* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_check_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  // the lookup made the device's context current if none was; cache under it
+  if (current_context_id(&id)) {
+    const int slot = g_scratch_cached < kCachedContexts ? g_scratch_cached++
+                                                        : (int)(id % kCachedContexts);
+    g_scratch_cache[slot] = {id, p};
   }
   *out = p;
   return cudaSuccess;
@@ -92,11 +143,14 @@ extern "C" int64_t nm_check_masks_noalloc(const uint32_t* masks, int64_t rows, i
   if (!masks) return -NM_ERR_NULL;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return -NM_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(masks) & 3u) != 0) return -NM_ERR_ALIGN;
-  const int64_t n = rows * (cols / 32);
-  if (n > NM_CHECK_NOALLOC_MAX_WORDS) return -NM_ERR_WORKSPACE;
+  // bound before multiplying, so that no product can wrap past the limit
+  const int64_t words = cols / 32;
+  if (words > NM_CHECK_NOALLOC_MAX_WORDS || rows > NM_CHECK_NOALLOC_MAX_WORDS / words)
+    return -NM_ERR_WORKSPACE;
+  const int64_t n = rows * words;
   if (n == 0) return 0;
   unsigned long long* scratch = nullptr;
-  if (scratch_on_current_device(&scratch) != cudaSuccess) return -NM_ERR_CUDA;
+  if (scratch_in_current_context(&scratch) != cudaSuccess) return -NM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int blocks = (int)((n + kWordsPerBlock - 1) / kWordsPerBlock);
   count_partial_kernel<<<blocks, kThreads, 0, s>>>(masks, n, scratch);

@@ -79,3 +79,24 @@ def test_library_has_no_oracle_dependency():
         assert "oracle" not in text.lower(), src
     import sparse_spmv_memory_gb300 as nm
     assert not hasattr(nm.lib(), "orc_matvec_f64")
+
+
+def test_oversize_shapes_are_refused_before_any_cuda_call():
+    """Shapes whose word count would wrap an int64 (or exceed the scratch of
+    the no-allocation check) are refused by the argument checks alone, so
+    these calls never reach the GPU: no device is needed to run them."""
+    import sparse_spmv_memory_gb300 as nm
+    L = nm.lib()
+    fake = 0x1000  # a 4-byte aligned, never dereferenced pointer
+    # rows * (cols / 32) wraps negative without the guard
+    wrap_rows, wrap_cols = 3 * 2**61 + 40_960_000, 64
+    assert L.nm_check_masks_noalloc(fake, wrap_rows, wrap_cols, None) == -5
+    assert L.nm_check_masks_noalloc(fake, 2**40, 2**40, None) == -5
+    assert L.nm_check_masks_noalloc(fake, 1, (67108864 + 1) * 32, None) == -5
+    assert L.nm_check_masks_noalloc(fake, 67108864 // 256 + 1, 256 * 32, None) == -5
+    assert L.nm_check_masks(fake, wrap_rows, wrap_cols, None) == -2
+    assert L.nm_check_masks(fake, 1024, 2**40, None) == -2
+    # the prefill entry points bound cols so the word count fits an int
+    assert nm.nm_spmm_prefill_workspace_bytes(128, 2**37, 64, 0, 1) == 0
+    assert L.nm_spmm_prefill_plan(128, 2**37, 64, 152, None, None, None) == 2
+    assert L.nm_spmm_prefill_plan(128, 8192, 64, 152, None, None, None) == 0
