@@ -121,15 +121,16 @@ class ClockSampler:
         self.dev = self.smi_id(device_index)
         self.proc = None
         self.path = None
-        self.window = [None, None]
+        self.windows = []  # [start, stop] of every timed region
 
     def start(self):
         import datetime
-        self.window[0] = datetime.datetime.now()
+        self.windows.append([datetime.datetime.now(), None])
 
     def stop(self):
         import datetime
-        self.window[1] = datetime.datetime.now()
+        if self.windows and self.windows[-1][1] is None:
+            self.windows[-1][1] = datetime.datetime.now()
 
     @staticmethod
     def smi_id(local: int) -> str:
@@ -149,7 +150,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -166,7 +167,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        """Clock samples taken between start() and stop() (all if unmarked)."""
+        """Clock samples taken inside the start()/stop() windows (all if unmarked)."""
         import datetime
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
@@ -181,9 +182,9 @@ class ClockSampler:
             except ValueError:
                 continue
         os.unlink(self.path)
-        t0, t1 = self.window
-        if t0 is not None and t1 is not None:
-            inside = [r for r in rows if t0 <= r[4] <= t1]
+        wins = [(a, b) for a, b in self.windows if a is not None and b is not None]
+        if wins:
+            inside = [r for r in rows if any(a <= r[4] <= b for a, b in wins)]
             rows = inside or rows
         if not rows:
             return None
@@ -408,6 +409,15 @@ class Step:
                 else:
                     torch.mm(self.x(l, i), W.t(), out=self.dense_out[i])
 
+    def run_cublas(self, slots):
+        """The batch-one sanity line: cuBLAS (torch.mm, a GEMV at one token)
+        on the same dense slots, x as a one-row matrix."""
+        import torch
+        for l in range(self.layers):
+            slot = slots[l % len(slots)]
+            for i, W in enumerate(slot):
+                torch.mm(self.x(l, i).view(1, -1), W.t(), out=self.y(l, i).view(1, -1))
+
     def bytes_sparse(self):
         B = self.batch
         # a fused SwiGLU call writes rows/2 outputs instead of rows
@@ -431,9 +441,10 @@ class Step:
         return self.layers * (len(self.mats) + extra)
 
 
-def time_graph(fn, steps, warmup, stream, clock=None):
+def time_graph(fn, steps, warmup, stream, clock=None, seconds=None):
     """Capture fn() in a CUDA graph, replay `warmup` times, then time `steps`
-    replays with CUDA events on `stream`.  Returns per-step ms and total s."""
+    replays with CUDA events on `stream` (steps None: as many as fill about
+    `seconds`, from a 3-replay estimate).  Returns per-step ms and total s."""
     import torch
     with torch.cuda.stream(stream):
         fn()  # eager once: plan caches and function attributes before capture
@@ -445,6 +456,16 @@ def time_graph(fn, steps, warmup, stream, clock=None):
         for _ in range(warmup):
             g.replay()
     torch.cuda.synchronize()
+    if steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(3):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        est = e0.elapsed_time(e1) / 3e3
+        steps = int(min(2000, max(5, (seconds or 0.5) / max(est, 1e-6))))
     barrier()
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
@@ -480,6 +501,86 @@ def time_per_matrix(step, slots, stream, reps):
     return out
 
 
+# The other decode-layer workloads the headline line also reports (the
+# pattern sweep under all four patterns, the 32B layer under 2:4 and 16:32).
+SIDE_PATTERNS = {"single_4096": [(2, 4)], "llama31_8b_layer": [(2, 4)],
+                 "pattern_sweep": PATTERNS, "qwen3_32b_layer": [(2, 4), (16, 32)],
+                 "llama33_70b_layer": PATTERNS}
+
+
+def spmv_kernel_label(nm, rows, cols):
+    """Which kernel and plan the library runs for one nm_spmv call."""
+    v, g, w = nm.nm_spmv_plan(rows, cols)
+    kern = "spmv_full_kernel" if cols % 1024 == 0 else "spmv_kernel"
+    return f"{kern} (nm_spmv plan: variant {v}, {w} warps x {g} blocks)"
+
+
+def time_dense_lines(step, dslots, stream, args, clock):
+    """dense_gemv and cuBLAS on the same dense slots: (ms per step) each."""
+    dper, dtotal = time_graph(lambda: step.run_dense(dslots), None, args.warmup, stream,
+                              clock=clock, seconds=args.side_seconds)
+    cper, ctotal = time_graph(lambda: step.run_cublas(dslots), None, args.warmup, stream,
+                              clock=clock, seconds=args.side_seconds)
+    return dtotal / len(dper) * 1e3, ctotal / len(cper) * 1e3
+
+
+def measure_side(nm, wname, device, stream, args, peak, clock):
+    """One more decode-layer workload, batch one: the whole step through
+    nm_spmv for each of its patterns, dense_gemv and cuBLAS on the same shapes,
+    and the µs per call of every matrix (graphs of one matrix, CUDA events)."""
+    import torch
+    mats, layers = WORKLOADS[wname], LAYERS[wname]
+    dense, xs = make_dense(mats, device, 1)
+    step = Step(nm, mats, layers, device)
+    step.fill_x(xs)
+    step_bytes = step.bytes_sparse()
+    out = {"shapes": ", ".join(f"{n} {r}x{c}" for n, r, c in mats), "layers": layers,
+           "physical_slots": args.slots, "patterns": {}}
+    per_call = None
+    for pat in SIDE_PATTERNS[wname]:
+        slots = pack_slots(nm, dense, pat, args.slots)
+        per, total = time_graph(lambda: step.run_sparse(slots), None, args.warmup, stream,
+                                clock=clock, seconds=args.side_seconds)
+        ms = total / len(per) * 1e3
+        out["patterns"][f"{pat[0]}:{pat[1]}"] = {"ms_per_step": round(ms, 4),
+                                                 "GB_s": round(step_bytes / ms / 1e6, 1)}
+        if per_call is None:
+            per_call = time_per_matrix(step, slots, stream, 10)
+        del slots
+        torch.cuda.empty_cache()
+    dslots = dense_slots(dense, args.dense_slots)
+    d_ms, c_ms = time_dense_lines(step, dslots, stream, args, clock)
+    del dslots, dense
+    torch.cuda.empty_cache()
+    head = out["patterns"]["2:4"]
+    best_dense = min(d_ms, c_ms)
+    out.update({
+        "GB_s": head["GB_s"], "frac_of_measured_peak": round(head["GB_s"] / peak, 4),
+        "ms_per_step": head["ms_per_step"],
+        "dense_gemv": {"ms_per_step": round(d_ms, 4),
+                       "GB_s": round(step.bytes_dense() / d_ms / 1e6, 1)},
+        "cublas": {"ms_per_step": round(c_ms, 4),
+                   "GB_s": round(step.bytes_dense() / c_ms / 1e6, 1),
+                   "kernel": "torch.mm (cuBLAS) on the dense weights, one token"},
+        "speedup_vs_dense": round(best_dense / head["ms_per_step"], 4),
+        "speedup_vs_dense_basis": "the faster of dense_gemv and cuBLAS",
+        "speedup_ideal": round(step.bytes_dense() / step_bytes, 4),
+    })
+    for k, v in out["patterns"].items():
+        v["speedup_vs_dense"] = round(best_dense / v["ms_per_step"], 4)
+    if len(out["patterns"]) > 1:
+        g = [v["GB_s"] for v in out["patterns"].values()]
+        out["pattern_spread"] = round((max(g) - min(g)) / statistics.median(g), 4)
+    out["us_per_call"] = {}
+    for i, (name, rows, cols) in enumerate(mats):
+        mu = statistics.median(per_call[i])
+        out["us_per_call"][name] = {"shape": f"{rows}x{cols}", "us_per_call": round(mu, 2),
+                                    "GB_s": round(sparse_bytes(rows, cols) / mu / 1e3, 1),
+                                    "frac_of_measured_peak":
+                                        round(sparse_bytes(rows, cols) / mu / 1e3 / peak, 4)}
+    return out
+
+
 def run_gpu(args):
     import torch
     import sparse_spmv_memory_gb300 as nm
@@ -504,17 +605,16 @@ def run_gpu(args):
     patterns = [head] + ([p for p in PATTERNS if p != head] if args.patterns else [])
     results = {}
     per_launch = None
-    clocks = None
+    cs = ClockSampler(local).__enter__()
     for pat in patterns:
         slots = pack_slots(nm, dense, pat, args.slots)
         fn = lambda: step.run_sparse(slots)
         if pat == head:
-            with ClockSampler(local) as cs:
-                per, total = time_graph(fn, args.steps, args.warmup, stream, clock=cs)
-            clocks = cs.summary()
+            per, total = time_graph(fn, args.steps, args.warmup, stream, clock=cs)
             per_launch = time_per_matrix(step, slots, stream, 10)
         else:
-            per, total = time_graph(fn, max(3, args.steps // 4), max(3, args.warmup), stream)
+            per, total = time_graph(fn, max(3, args.steps // 4), max(3, args.warmup), stream,
+                                    clock=cs)
         results[pat] = (per, total, len(per))
         del slots, fn
         torch.cuda.empty_cache()
@@ -547,15 +647,31 @@ def run_gpu(args):
     del slots
     torch.cuda.empty_cache()
 
-    # dense baseline on the same shapes and rotation scheme
-    dense_res = None
+    # dense baselines on the same shapes and rotation scheme: the library's own
+    # dense_gemv, and cuBLAS as the sanity line (batch one)
+    dense_res = cublas_ms = None
     if args.dense:
         dslots = dense_slots(dense, args.dense_slots)
         dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
-                                  args.warmup, stream)
+                                  args.warmup, stream, clock=cs)
         dense_res = (dper, dtotal, len(dper))
+        if args.batch == 1:
+            cper, ctotal = time_graph(lambda: step.run_cublas(dslots), max(3, args.steps // 2),
+                                      args.warmup, stream, clock=cs)
+            cublas_ms = ctotal / len(cper) * 1e3
         del dslots
         torch.cuda.empty_cache()
+    del dense
+    torch.cuda.empty_cache()
+
+    # the other decode-layer workloads, batch one, on the same line
+    side = {}
+    if args.side and args.batch == 1 and not args.swiglu:
+        for wname in WORKLOADS:
+            if wname != args.workload:
+                side[wname] = measure_side(nm, wname, device, stream, args, peak, cs)
+    cs.__exit__(None, None, None)
+    clocks = cs.summary()
 
     # ---- assemble ------------------------------------------------------------
     per, total, k = results[head]
@@ -603,25 +719,33 @@ def run_gpu(args):
         mu = statistics.median(us)
         calls[name] = {"shape": f"{rows}x{cols}", "us_per_call": round(mu, 2),
                        "GB_s": round(sparse_bytes(rows, cols) / mu / 1e3, 1),
+                       "frac_of_measured_peak": round(sparse_bytes(rows, cols) / mu / 1e3 / peak, 4),
                        "bytes": sparse_bytes(rows, cols)}
     out["us_per_call"] = calls
-    # The only kernel in the timed region is nm_spmv; its average launch
-    # duration is bounded above by the region's device time / launches, so
-    # this achieved figure is a lower bound on the kernel's own rate.
-    achieved = step_bytes * k / total / 1e9
-    dom = max(mats, key=lambda m: sparse_bytes(m[1], m[2]))
+    # The dominant kernel is the launch that moves the most bytes (gate+up on
+    # the decode layers): its algorithmic bytes per launch over its average
+    # launch duration, from CUDA events around a graph of back-to-back
+    # launches of that matrix alone on the launching stream.
+    di, dom = max(enumerate(mats), key=lambda im: sparse_bytes(im[1][1], im[1][2]))
+    dom_bytes = sparse_bytes(dom[1], dom[2])
+    dom_us = statistics.median(per_launch[di])
+    achieved = dom_bytes / dom_us / 1e3
     traffic = ncu_traffic(f"{dom[1]}x{dom[2]}")
     out["roofline"] = {
-        "bound": "hbm", "kernel": "nm_spmv (spmv_kernel)",
-        "achieved": None if achieved is None else round(achieved, 1),
-        "peak": peak, "unit": "GB/s",
-        "frac": None if achieved is None else round(achieved / peak, 4),
+        "bound": "hbm", "kernel": "nm_spmv: " + spmv_kernel_label(nm, dom[1], dom[2]),
+        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
         "traffic": traffic,
         "traffic_shape": f"{dom[1]}x{dom[2]}",
-        "traffic_algorithmic": sparse_bytes(dom[1], dom[2]),
-        "achieved_basis": ("algorithmic bytes of the timed region's nm_spmv launches / the "
-                           "region's CUDA-event device time (launch gaps included: a lower bound)"),
+        "traffic_algorithmic": dom_bytes,
+        "achieved_basis": (f"algorithmic bytes of one {dom[1]}x{dom[2]} launch ({dom_bytes} B: "
+                           "values + masks + x + y) / its average launch duration "
+                           f"({dom_us:.2f} us, CUDA events around a graph of {layers} "
+                           "back-to-back launches over the rotating slots)"),
+        "step_frac": round(gbs / world / peak, 4),
+        "step_frac_basis": ("the whole step's algorithmic bytes / the step's CUDA-event time, "
+                            "launch gaps and the smaller matrices included"),
     }
     out["patterns"] = {
         f"{p[0]}:{p[1]}": {"ms_per_step": round(results[p][1] / results[p][2] * 1e3, 4),
@@ -636,8 +760,22 @@ def run_gpu(args):
                         "GB_s": round(step.bytes_dense() * dk / dtotal / 1e9, 1),
                         "physical_slots": args.dense_slots,
                         "kernel": "dense_gemv" if args.batch == 1 else "cuBLAS via torch.mm"}
-        out["speedup_vs_dense"] = round(d_ms / (total / k * 1e3), 4)
+        best = d_ms
+        if cublas_ms is not None:
+            out["cublas"] = {"ms_per_step": round(cublas_ms, 4),
+                             "GB_s": round(step.bytes_dense() / cublas_ms / 1e6, 1),
+                             "kernel": "torch.mm (cuBLAS) on the dense weights, one token"}
+            best = min(d_ms, cublas_ms)
+            out["speedup_vs_cublas"] = round(cublas_ms / (total / k * 1e3), 4)
+        out["speedup_vs_dense"] = round(best / (total / k * 1e3), 4)
+        out["speedup_vs_dense_basis"] = ("the faster of dense_gemv and cuBLAS"
+                                         if cublas_ms is not None else "dense_gemv")
         out["speedup_ideal"] = round(step.bytes_dense() / step_bytes, 4)
+        for p in patterns:
+            out["patterns"][f"{p[0]}:{p[1]}"]["speedup_vs_dense"] = round(
+                best / (results[p][1] / results[p][2] * 1e3), 4)
+    if side:
+        out["workloads"] = side
     xb = step.x_all.numel() * 2
     yb = step.y_all.numel() * 2
     e_units, e_secs = aggregate(step_bytes * args.steps, e2e_s)
@@ -920,6 +1058,10 @@ def parse(argv=None):
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-patterns", dest="patterns", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--no-side", dest="side", action="store_false",
+                    help="skip the other decode-layer workloads (reported under 'workloads')")
+    ap.add_argument("--side-seconds", type=float, default=0.4,
+                    help="timed seconds per measurement of each other workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--flags", type=int, default=-1,
                     help="launch flags for every call (default: the library's own, i.e. "

@@ -70,19 +70,22 @@ __device__ __forceinline__ void fma8(const uint4& w, const uint4& x, float& a0, 
 }
 
 template <int NW, int U>
-__global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(NW * 32, 1) nm_dense_matvec_kernel(const GemvParams p) {
   extern __shared__ __align__(16) uint4 gsmem[];
   const int T = p.steps;
-  uint4* xs = gsmem;                                   // [T*64] x as fp16, zero padded
+  uint4* xs = gsmem;                                     // [T*64] x as fp16, zero padded
   float* pf = reinterpret_cast<float*>(gsmem + T * 64);  // [NW]
-  float* pl = pf + NW;                                 // [NW]
+  float* pl = pf + NW;                                   // [NW]
+  int* rinfo = reinterpret_cast<int*>(pl + NW);          // [NW][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BlockRows br = block_rows(p.rows);
+  const BlockRows br = block_rows(p.rows_q, p.rows_r);
   const int64_t F = (br.r1 - br.r0) * T;
   const WarpRange wr = warp_range<NW>(F, warp);
+  const int64_t row0 = div_steps(wr.sb, T);
+  const int t0 = (int)(wr.sb - row0 * T);
 
-  GemvCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  GemvCursor lc{wr.sb, row0, t0};
   GemvBatch<U> A, B;
   pdl_launch_dependents();
   if (!p.early_weights) pdl_wait_previous();
@@ -94,8 +97,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
   }
   __syncthreads();
 
-  auto store = [&](int64_t row, float v) { p.y[br.r0 + row] = __float2half_rn(v); };
-  GemvCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  auto store = [&](int row, float v) { p.y[br.r0 + row] = __float2half_rn(v); };
+  GemvCursor cc{wr.sb, row0, t0};
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 
   auto compute = [&](GemvBatch<U>& bt) {
@@ -108,7 +111,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
         fma8(bt.w[i][1], x1, a2, a3);
         if (cc.t == T - 1 || cc.s == wr.se - 1) {
           const float v = warp_sum((a0 + a1) + (a2 + a3));
-          finish_row(cc.row, v, wr, T, warp, lane, pf, pl, store);
+          const bool whole = cc.t == T - 1 && (cc.row != row0 || t0 == 0);
+          finish_row((int)cc.row, v, whole, (int)row0, warp, lane, pf, pl, store);
           a0 = a1 = a2 = a3 = 0.f;
         }
         advance(cc, T);
@@ -123,19 +127,24 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
     gemv_load<U>(A, lc, wr.se, T, p, br.r0, lane);
     compute(B);
   }
+  note_range(rinfo, warp, lane, wr.se > wr.sb ? (int)row0 : -1, t0 != 0,
+             (int)(cc.t != 0 ? cc.row : cc.row - 1), cc.t != 0);
 
   __syncthreads();
-  combine_cut_rows<NW>(F, T, pf, pl, store);
+  combine_cut_rows<NW>(rinfo, pf, pl, store);
 }
 
 size_t gemv_smem_bytes(int steps, int nw) {
-  return (size_t)steps * 64 * sizeof(uint4) + 2 * (size_t)nw * sizeof(float);
+  return (size_t)steps * 64 * sizeof(uint4) + 6 * (size_t)nw * sizeof(float);
 }
 
 template <int NW, int U>
-static cudaError_t launch_gemv_t(const GemvParams& p, int grid, int flags, cudaStream_t stream) {
+static cudaError_t launch_gemv_t(const GemvParams& p0, int grid, int flags, cudaStream_t stream) {
   static int smem_set[64] = {0};
-  auto* k = gemv_kernel<NW, U>;
+  GemvParams p = p0;
+  p.rows_q = p.rows / grid;
+  p.rows_r = (int)(p.rows % grid);
+  auto* k = nm_dense_matvec_kernel<NW, U>;
   cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
   if (e != cudaSuccess) return e;
   return launch_kernel(k, grid, NW * 32, gemv_smem_bytes(p.steps, NW), stream, flags, p);

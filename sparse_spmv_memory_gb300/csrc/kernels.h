@@ -19,6 +19,8 @@ struct SpmvParams {
   int steps;  // ceil(words / 32): warp-steps per row
   int pitch;  // floats per row of the transposed x tile (multiple of 32, >= words)
   int early_weights;  // 1: load the first weights before waiting on the previous kernel
+  int64_t rows_q = 0;  // set by the launcher: rows (or row pairs) per block ...
+  int rows_r = 0;      // ... and how many blocks take one more
 };
 
 struct SpmvPlan {
@@ -45,6 +47,8 @@ struct GemvParams {
   int cols;
   int steps;  // ceil(cols / 512)
   int early_weights;
+  int64_t rows_q = 0;  // set by the launcher: rows per block, blocks with one more
+  int rows_r = 0;
 };
 
 struct GemvPlan {
@@ -75,6 +79,11 @@ struct SpmmParams {
   int pitch;   // x-tile slots per row (>= 32 * steps of the widest slice)
   int batch;   // 1..8
   int early_weights;
+  int64_t rows_q = 0;  // set by the launcher: rows per block of a slice, blocks with one more
+  int rows_r = 0;
+  int bps = 1;         // blocks per column slice
+  int steps_q = 0;     // steps per slice, and how many slices take one more
+  int steps_r = 0;
 };
 
 struct SpmmPlan {

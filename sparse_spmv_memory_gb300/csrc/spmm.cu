@@ -237,20 +237,23 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   float* tile_f = smem;                                 // [34][P][BP] fp32 (XF 1)
   float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
   float* pl = pf + NW * BP;                             // [NW][BP]
+  int* rinfo = reinterpret_cast<int*>(pl + NW * BP);    // [NW][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bps = gridDim.x / p.slices;  // blocks per slice
-  const int sl = blockIdx.x / bps, c = blockIdx.x - sl * bps;
-  const int64_t r0 = p.rows * c / bps, r1 = p.rows * (c + 1) / bps;
-  const int ts0 = (int)((int64_t)p.steps * sl / p.slices);
-  const int ts1 = (int)((int64_t)p.steps * (sl + 1) / p.slices);
+  const int sl = (int)(blockIdx.x / (unsigned)p.bps), c = blockIdx.x - sl * p.bps;  // slice, block in it
+  const BlockRows br = split_part(c, p.rows_q, p.rows_r, p.bps);
+  const int64_t r0 = br.r0, r1 = br.r1;
+  const BlockRows sr = split_part(sl, p.steps_q, p.steps_r, p.slices);
+  const int ts0 = (int)sr.r0, ts1 = (int)sr.r1;
   const int T = ts1 - ts0;              // warp-steps per row in this slice
   const int w0 = ts0 * 32;              // first mask word of the slice
   const int wend = min(ts1 * 32, p.words);
   const int64_t F = (r1 - r0) * T;
   const WarpRange wr = warp_range<NW>(F, warp);
+  const int64_t row0 = div_steps(wr.sb, T);
+  const int t0 = (int)(wr.sb - row0 * T);
 
-  SpmmCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  SpmmCursor lc{wr.sb, row0, t0};
   SpmmBatch<U> A, B;
   pdl_launch_dependents();
   if (!p.early_weights) pdl_wait_previous();
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   const uint32_t row_bytes = (uint32_t)P * kSlotWords * 4u;
   const uint32_t swz = ((lane >> 2) & 1) ? 16u : 0u;  // local word bit 2 == lane bit 2
   const uint32_t tile_base = smem_addr(tile) + row_bytes;  // row b = 0
-  auto store = [&](int64_t row, const float (&v)[BP]) {
+  auto store = [&](int row, const float (&v)[BP]) {
     const int64_t gr = r0 + row;
     if (p.slices == 1) {
 #pragma unroll
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
     }
   };
 
-  SpmmCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  SpmmCursor cc{wr.sb, row0, t0};
   float a[2][BP];                   // XF 0
   unsigned long long a2[2][BP / 2];  // XF 1: packed pairs of tokens
 #pragma unroll
@@ -344,7 +347,8 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
           }
 #pragma unroll
           for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
-          finish_row_n<BP>(cc.row, v, wr, T, warp, lane, pf, pl, store);
+          const bool whole = cc.t == T - 1 && (cc.row != row0 || t0 == 0);
+          finish_row_n<BP>((int)cc.row, v, whole, (int)row0, warp, lane, pf, pl, store);
         }
         advance(cc, T);
       }
@@ -359,8 +363,11 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
     compute(B);
   }
 
+  note_range(rinfo, warp, lane, wr.se > wr.sb ? (int)row0 : -1, t0 != 0,
+             (int)(cc.t != 0 ? cc.row : cc.row - 1), cc.t != 0);
+
   __syncthreads();
-  combine_cut_rows_n<NW, BP>(F, T, pf, pl, store);
+  combine_cut_rows_n<NW, BP>(rinfo, pf, pl, store);
 }
 
 // Y[j][r] = sum over slices s (in order) of partial[s][j][r], rounded to fp16.
@@ -369,18 +376,19 @@ __global__ void __launch_bounds__(256) spmm_combine_kernel(const float* __restri
                                                            __half* __restrict__ Y, int64_t ldy) {
   pdl_launch_dependents();
   pdl_wait_previous();
-  const int64_t n = (int64_t)batch * rows;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t j = i / rows, r = i - j * rows;
-    float s = 0.f;
-    for (int k = 0; k < slices; ++k) s += partial[((int64_t)k * batch + j) * rows + r];
-    Y[j * ldy + r] = __float2half_rn(s);
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    for (int j = 0; j < batch; ++j) {
+      float s = 0.f;
+      for (int k = 0; k < slices; ++k) s += partial[((int64_t)k * batch + j) * rows + r];
+      Y[j * ldy + r] = __float2half_rn(s);
+    }
   }
 }
 
 size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf) {
-  return (size_t)34 * pitch * bp * (xf ? 4 : 2) + 2 * (size_t)nw * bp * sizeof(float);
+  return (size_t)34 * pitch * bp * (xf ? 4 : 2) + 2 * (size_t)nw * bp * sizeof(float) +
+         4 * (size_t)nw * sizeof(int);
 }
 
 int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8); }
@@ -425,8 +433,14 @@ static cudaError_t launch_spmm_bp(const SpmmParams& p, int bp, int grid, int fla
   }
 }
 
-cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
+cudaError_t launch_spmm(const SpmmParams& p0, const SpmmPlan& plan, int flags,
                         cudaStream_t stream) {
+  SpmmParams p = p0;
+  p.bps = plan.grid / p.slices;  // the plan's grid is a whole number of blocks per slice
+  p.rows_q = p.rows / p.bps;
+  p.rows_r = (int)(p.rows % p.bps);
+  p.steps_q = p.steps / p.slices;
+  p.steps_r = p.steps % p.slices;
   cudaError_t e;
   switch (plan.variant) {
 #define NM_SPMM_CASE(i)                                                                 \

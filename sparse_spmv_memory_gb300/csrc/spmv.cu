@@ -194,18 +194,21 @@ template <int NW, int U, int DEC, int EPI>
 __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;
-  float* xs = smem;           // [34][P]
-  float* pf = smem + 34 * P;  // [NW] first-row partials
-  float* pl = pf + NW;        // [NW] last-row partials
-  float* ysm = pl + NW;       // EPI 1: fp32 sums of the block's rows
+  float* xs = smem;                                    // [34][P]
+  float* pf = smem + 34 * P;                           // [NW] first-row partials
+  float* pl = pf + NW;                                 // [NW] last-row partials
+  int* rinfo = reinterpret_cast<int*>(pl + NW);        // [NW][4] rows each warp touches
+  float* ysm = reinterpret_cast<float*>(rinfo + 4 * NW);  // EPI 1: fp32 sums of the block's rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.steps;
-  const BlockRows br = EPI ? block_row_pairs(p.rows) : block_rows(p.rows);
+  const BlockRows br = EPI ? block_row_pairs(p.rows_q, p.rows_r) : block_rows(p.rows_q, p.rows_r);
   const int64_t F = (br.r1 - br.r0) * T;
   const WarpRange wr = warp_range<NW>(F, warp);
+  const int64_t row0 = div_steps(wr.sb, T);
+  const int t0 = (int)(wr.sb - row0 * T);
 
-  SpmvCursor lc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  SpmvCursor lc{wr.sb, row0, t0};
   SpmvBatch<U> A, B;
   pdl_launch_dependents();
   if (!p.early_weights) pdl_wait_previous();
@@ -217,14 +220,14 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
 
   const uint32_t xs_base = smem_addr(xs);
   const uint32_t row_bytes = 4u * (uint32_t)P;
-  auto store = [&](int64_t row, float v) {
+  auto store = [&](int row, float v) {
     if (EPI)
       ysm[row] = v;
     else
       p.y[br.r0 + row] = __float2half_rn(v);
   };
 
-  SpmvCursor cc{wr.sb, wr.sb / T, (int)(wr.sb % T)};
+  SpmvCursor cc{wr.sb, row0, t0};
   float a0 = 0.f, a1 = 0.f;
 
   auto compute = [&](SpmvBatch<U>& bt) {
@@ -235,7 +238,8 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
         decode_word<DEC>(bt.m[i], bt.v[i], col_addr, row_bytes, a0, a1);
         if (cc.t == T - 1 || cc.s == wr.se - 1) {
           const float v = warp_sum(a0 + a1);
-          finish_row(cc.row, v, wr, T, warp, lane, pf, pl, store);
+          const bool whole = cc.t == T - 1 && (cc.row != row0 || t0 == 0);
+          finish_row((int)cc.row, v, whole, (int)row0, warp, lane, pf, pl, store);
           a0 = 0.f;
           a1 = 0.f;
         }
@@ -251,9 +255,12 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_kernel(const SpmvParams p) {
     spmv_load<U>(A, lc, wr.se, T, p, br.r0, lane);
     compute(B);
   }
+  // cc now points just past the range: a nonzero step means the range ends inside a row
+  note_range(rinfo, warp, lane, wr.se > wr.sb ? (int)row0 : -1, t0 != 0,
+             (int)(cc.t != 0 ? cc.row : cc.row - 1), cc.t != 0);
 
   __syncthreads();
-  combine_cut_rows<NW>(F, T, pf, pl, store);
+  combine_cut_rows<NW>(rinfo, pf, pl, store);
   if (EPI) swiglu_epilogue<NW>(ysm, br.r0, br.r1, p.y);
 }
 
@@ -283,11 +290,12 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
   float* xs = smem;
   float* pf = smem + 34 * P;
   float* pl = pf + NW;
-  float* ysm = pl + NW;  // EPI 1
+  int* rinfo = reinterpret_cast<int*>(pl + NW);
+  float* ysm = reinterpret_cast<float*>(rinfo + 4 * NW);  // EPI 1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.steps;
-  const BlockRows br = EPI ? block_row_pairs(p.rows) : block_rows(p.rows);
+  const BlockRows br = EPI ? block_row_pairs(p.rows_q, p.rows_r) : block_rows(p.rows_q, p.rows_r);
   const int F = (int)((br.r1 - br.r0) * T);
   const WarpRange wr = warp_range<NW>(F, warp);
   const int sb = (int)wr.sb, se = (int)wr.se;
@@ -307,14 +315,15 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
 
   const uint32_t row_bytes = 4u * (uint32_t)P;
   const uint32_t lane_col = smem_addr(xs) + row_bytes + 4u * (uint32_t)lane;
-  auto store = [&](int64_t row, float v) {
+  auto store = [&](int row, float v) {
     if (EPI)
       ysm[row] = v;
     else
       p.y[br.r0 + row] = __float2half_rn(v);
   };
 
-  int row = sb / T, t = sb - row * T;
+  const int row0 = sb / T, t0 = sb - row0 * T;
+  int row = row0, t = t0;
   uint32_t col_addr = lane_col + 128u * (uint32_t)t;
   float a0 = 0.f, a1 = 0.f;
 
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
     decode_word<DEC>(m, v, col_addr, row_bytes, a0, a1);
     col_addr += 128u;
     if (++t == T) {  // row complete
-      finish_row(row, warp_sum(a0 + a1), wr, T, warp, lane, pf, pl, store);
+      finish_row(row, warp_sum(a0 + a1), row != row0 || t0 == 0, row0, warp, lane, pf, pl, store);
       a0 = 0.f;
       a1 = 0.f;
       t = 0;
@@ -346,20 +355,25 @@ __global__ void __launch_bounds__(NW * 32, 1) spmv_full_kernel(const SpmvParams 
     step(one.m[0], one.v[0]);
   }
   if (se > sb && t != 0)  // the warp's range ends inside a row
-    finish_row(row, warp_sum(a0 + a1), wr, T, warp, lane, pf, pl, store);
+    finish_row(row, warp_sum(a0 + a1), false, row0, warp, lane, pf, pl, store);
+  note_range(rinfo, warp, lane, se > sb ? row0 : -1, t0 != 0, t != 0 ? row : row - 1, t != 0);
 
   __syncthreads();
-  combine_cut_rows<NW>(F, T, pf, pl, store);
+  combine_cut_rows<NW>(rinfo, pf, pl, store);
   if (EPI) swiglu_epilogue<NW>(ysm, br.r0, br.r1, p.y);
 }
 
 size_t spmv_smem_bytes(int pitch, int nw) {
-  return (size_t)(34 * pitch + 2 * nw) * sizeof(float);
+  return (size_t)(34 * pitch + 6 * nw) * sizeof(float);  // x tile, pf, pl, rinfo
 }
 
 template <int NW, int U, int DEC, int EPI>
-static cudaError_t launch_spmv_e(const SpmvParams& p, int grid, int flags, cudaStream_t stream) {
+static cudaError_t launch_spmv_e(const SpmvParams& p0, int grid, int flags, cudaStream_t stream) {
   static int smem_full[64] = {0}, smem_gen[64] = {0};
+  SpmvParams p = p0;
+  const int64_t units = EPI ? p.rows / 2 : p.rows;  // rows, or (gate, up) pairs
+  p.rows_q = units / grid;
+  p.rows_r = (int)(units % grid);
   const int64_t block_rows_max = EPI ? 2 * ((p.rows / 2 + grid - 1) / grid) : 0;
   const size_t smem = spmv_smem_bytes(p.pitch, NW) + (size_t)block_rows_max * sizeof(float);
   const int64_t block_steps = ((p.rows + grid - 1) / grid + 2) * p.steps;

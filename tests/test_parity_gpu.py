@@ -340,45 +340,3 @@ def test_argument_errors(nm):
         nm.nm_spmv(v.cpu(), m.cpu(), x_cpu := torch.zeros(cols, dtype=torch.float16))
     torch.cuda.synchronize()
     assert torch.equal(v, nm.nm_pack(Wd, 2, 4)[0])  # rejected calls wrote nothing
-
-
-# ---------------------------------------------------------------------------
-# the full decode-layer workloads, in the benchmark's launch configuration
-# ---------------------------------------------------------------------------
-def sample_ids(rows, grid):
-    ids = set(synth.sample_rows(rows, 40, 0, synth.stream_id(16, rows)).tolist())
-    for c in range(1, grid, max(1, grid // 12)):   # rows at block boundaries
-        b = rows * c // grid
-        ids.update({b - 1, b})
-    return np.array(sorted(i for i in ids if 0 <= i < rows), dtype=np.int64)
-
-
-@pytest.mark.parametrize("workload", list(WORKLOADS))
-def test_full_size_workload(nm, orc, workload):
-    spec = WORKLOADS[workload]
-    for mi, (name, (rows, cols)) in enumerate(spec["mats"].items()):
-        W = synth.weights(rows, cols, 0, synth.stream_id(2, mi, 0))
-        x = synth.activations(cols, 0, synth.stream_id(2, mi, 1))
-        Wd, xd = to_dev(W), to_dev(x)
-        _, grid, _ = nm.nm_spmv_plan(rows, cols)
-        ids = sample_ids(rows, grid)
-        Ws = np.ascontiguousarray(W[ids])
-        sizes = set()
-        for N, M in spec["patterns"]:
-            v, m = nm.nm_pack(Wd, N, M)
-            assert nm.nm_check_masks(m, cols) == 0
-            sizes.add((v.numel() * 2, m.numel() * 4))
-            ov, om = orc.prune_pack(Ws, N, M)
-            idt = torch.from_numpy(ids).cuda()
-            assert np.array_equal(from_dev(m.index_select(0, idt)), om), (name, N, M)
-            assert np.array_equal(from_dev(v.index_select(0, idt)), ov), (name, N, M)
-            y = nm.nm_spmv(v, m, xd)
-            y_ref, s = orc.spmv_f64(ov, om, cols, x)
-            assert_within_tol(from_dev(y)[ids], y_ref, s, f"{workload}/{name} {N}:{M}")
-            del v, m, y
-        assert sizes == {(rows * cols, rows * cols // 8)}
-        yd = nm.dense_gemv(Wd, xd)
-        yd_ref, sd = orc.matvec_f64(Ws, x)
-        assert_within_tol(from_dev(yd)[ids], yd_ref, sd, f"{workload}/{name} dense")
-        del Wd, yd
-        torch.cuda.empty_cache()

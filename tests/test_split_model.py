@@ -1,67 +1,86 @@
 """CPU model of the row/step split used by the matrix-vector kernels.
 
-Mirrors the index arithmetic of csrc/split.cuh (block row ranges, per-warp
-step ranges, which warp finishes which row, and the ordered sum of rows cut
-between warps) and checks, for many shapes and launch sizes, that every
-(row, step) is read exactly once, every row is written exactly once, and
-every load stays inside the packed arrays.  Run before the kernels ever see
-a GPU; the GPU parity tests then check the kernels themselves.
+Mirrors the index arithmetic of csrc/split.cuh (block row ranges from a
+quotient/remainder split, per-warp step ranges, the per-warp record of the
+rows a range touches, which warp finishes which row, and the ordered sum of
+rows cut between warps) and checks, for many shapes and launch sizes, that
+every (row, step) is read exactly once, every row is written exactly once,
+and every load stays inside the packed arrays.  Run before the kernels ever
+see a GPU; the GPU parity tests then check the kernels themselves.
 """
 import itertools
 
 import pytest
 
 
+def split_at(c, n, parts):
+    """split.cuh's floor(n * c / parts) as the kernels compute it: with
+    n = q * parts + r, c * q + floor(c * r / parts)."""
+    q, r = divmod(n, parts)
+    return c * q + (c * r) // parts
+
+
+def split_part(c, n, parts):
+    return split_at(c, n, parts), split_at(c + 1, n, parts)
+
+
 def block_rows(rows, G, c):
-    return rows * c // G, rows * (c + 1) // G
+    return split_part(c, rows, G)
 
 
 def warp_range(F, NW, w):
-    return F * w // NW, F * (w + 1) // NW
+    return split_part(w, F, NW)
+
+
+def combine(NW, rinfo, pf, pl, r0, writes):
+    """combine_cut_rows: thread t sums the row its warp cuts at its end, if
+    the row started inside warp t, with the following warps' first-row
+    partials up to the warp that reaches the row's end."""
+    for t_ in range(NW):
+        first, cs, last, ce = rinfo[t_]
+        if first < 0 or not ce or (last == first and cs):
+            continue
+        total = list(pf[t_] if last == first else pl[t_])
+        for u in range(t_ + 1, NW):
+            if rinfo[u][0] < 0:
+                continue
+            total += pf[u]
+            if not (rinfo[u][3] and rinfo[u][2] == last):
+                break
+        writes.setdefault(r0 + last, []).append(sorted(total))
 
 
 def simulate(rows, T, G, NW):
+    """The general kernel's control flow (cursor over flattened steps)."""
     writes = {}
     reads = {}
     for c in range(G):
         r0, r1 = block_rows(rows, G, c)
         F = (r1 - r0) * T
-        pf, pl = {}, {}
+        pf, pl, rinfo = {}, {}, {}
         for w in range(NW):
             sb, se = warp_range(F, NW, w)
+            row0, t0 = divmod(sb, T)
+            row, t = row0, t0
             acc = []
             for s in range(sb, se):
-                row, t = divmod(s, T)
+                assert (row, t) == divmod(s, T)
                 reads[(r0 + row, t)] = reads.get((r0 + row, t), 0) + 1
                 acc.append((r0 + row, t))
                 if t == T - 1 or s == se - 1:
-                    beg, end = row * T, row * T + T
-                    if beg >= sb and end <= se:
+                    whole = t == T - 1 and (row != row0 or t0 == 0)
+                    if whole:
                         writes.setdefault(r0 + row, []).append(sorted(acc))
-                    elif row == sb // T:
+                    elif row == row0:
                         pf[w] = acc
                     else:
                         pl[w] = acc
                     acc = []
-        # combine_cut_rows
-        for t_ in range(NW):
-            sb, se = warp_range(F, NW, t_)
-            if sb == se:
-                continue
-            rf, rl = sb // T, (se - 1) // T
-            cut = se % T != 0
-            first = rl != rf or sb % T == 0
-            if not (cut and first):
-                continue
-            total = list(pf[t_] if rl == rf else pl[t_])
-            for u in range(t_ + 1, NW):
-                ub, ue = warp_range(F, NW, u)
-                if ub == ue:
-                    continue
-                total += pf[u]
-                if ue >= (rl + 1) * T:
-                    break
-            writes.setdefault(r0 + rl, []).append(sorted(total))
+                t += 1
+                if t == T:
+                    t, row = 0, row + 1
+            rinfo[w] = (row0 if se > sb else -1, t0 != 0, row if t != 0 else row - 1, t != 0)
+        combine(NW, rinfo, pf, pl, r0, writes)
     return reads, writes
 
 
@@ -73,18 +92,18 @@ def simulate_whole_step(rows, T, G, NW, U):
     for c in range(G):
         r0, r1 = block_rows(rows, G, c)
         F = (r1 - r0) * T
-        pf, pl = {}, {}
+        pf, pl, rinfo = {}, {}, {}
         for w in range(NW):
             sb, se = warp_range(F, NW, w)
-            row, t = divmod(sb, T)
+            row0, t0 = divmod(sb, T)
+            row, t = row0, t0
             acc = []
             steps = list(range(sb, sb + (se - sb) // U * U)) + list(range(sb + (se - sb) // U * U, se))
 
-            def finish(row, acc):
-                beg, end = row * T, row * T + T
-                if beg >= sb and end <= se:
+            def finish(row, acc, whole):
+                if whole:
                     writes.setdefault(r0 + row, []).append(sorted(acc))
-                elif row == sb // T:
+                elif row == row0:
                     pf[w] = acc
                 else:
                     pl[w] = acc
@@ -95,27 +114,24 @@ def simulate_whole_step(rows, T, G, NW, U):
                 acc.append((r0 + row, t))
                 t += 1
                 if t == T:
-                    finish(row, acc)
+                    finish(row, acc, row != row0 or t0 == 0)
                     acc, t, row = [], 0, row + 1
             if se > sb and t != 0:
-                finish(row, acc)
-        for t_ in range(NW):
-            sb, se = warp_range(F, NW, t_)
-            if sb == se:
-                continue
-            rf, rl = sb // T, (se - 1) // T
-            if not (se % T != 0 and (rl != rf or sb % T == 0)):
-                continue
-            total = list(pf[t_] if rl == rf else pl[t_])
-            for u in range(t_ + 1, NW):
-                ub, ue = warp_range(F, NW, u)
-                if ub == ue:
-                    continue
-                total += pf[u]
-                if ue >= (rl + 1) * T:
-                    break
-            writes.setdefault(r0 + rl, []).append(sorted(total))
+                finish(row, acc, False)
+            rinfo[w] = (row0 if se > sb else -1, t0 != 0, row if t != 0 else row - 1, t != 0)
+        combine(NW, rinfo, pf, pl, r0, writes)
     return reads, writes
+
+
+def test_split_at_is_the_floor_formula():
+    """The kernels' division-free form gives exactly floor(n * c / parts)."""
+    import random
+    rng = random.Random(5)
+    for _ in range(20000):
+        parts = rng.choice([1, 2, 3, 7, 24, 152, 304, 1000, 65535])
+        n = rng.choice([rng.randrange(0, 5000), rng.randrange(0, 2**31), rng.randrange(0, 2**40)])
+        c = rng.randrange(0, parts + 1)
+        assert split_at(c, n, parts) == n * c // parts
 
 
 SHAPES = [(1, 1), (1, 4), (3, 1), (7, 3), (33, 2), (300, 2), (257, 4), (1000, 5), (4096, 4),
@@ -180,8 +196,9 @@ def test_spmm_slices_cover_every_step_once(rows, T):
             reads, writes = {}, {}
             for b in range(G):
                 sl, c = divmod(b, bps)
-                r0, r1 = rows * c // bps, rows * (c + 1) // bps
-                ts0, ts1 = T * sl // S, T * (sl + 1) // S
+                r0, r1 = split_part(c, rows, bps)
+                ts0, ts1 = split_part(sl, T, S)
+                assert ts1 - ts0 <= -(-T // S)  # the widest slice fits the planned x tile
                 for r in range(r0, r1):
                     for t in range(ts0, ts1):
                         reads[(r, t)] = reads.get((r, t), 0) + 1

@@ -138,16 +138,3 @@ def test_spmm_long_rows_need_slices(nm):
     # batch 8 on the 70B down projection: the x tile of a whole row does not fit
     assert nm.nm_spmm_workspace_bytes(8192, 28672, 8) > 0
     assert nm.nm_spmm_workspace_bytes(8192, 8192, 2) == 0
-
-
-@pytest.mark.parametrize("rows,cols,batch", [(8192, 28672, 8), (57344, 8192, 4), (4096, 14336, 8)])
-def test_spmm_full_size_sampled_rows(nm, orc, rows, cols, batch):
-    W = synth.weights(rows, cols, 0, synth.stream_id(41, rows, cols))
-    X = synth.normal_f16((batch, cols), 0, synth.stream_id(42, rows, cols), synth.X_SIGMA)
-    v, m = nm.nm_pack(to_dev(W), 2, 4)
-    Y = from_dev(nm.nm_spmm(v, m, to_dev(X)))
-    ids = synth.sample_rows(rows, 48, 0, synth.stream_id(43, rows))
-    ov, om = orc.prune_pack(np.ascontiguousarray(W[ids]), 2, 4)
-    ref, s = oracle_spmm(orc, ov, om, cols, X)
-    err = np.abs(f16_to_f64(Y[:, ids]) - ref)
-    assert np.all(err <= oracle.tolerance(s)), err.max()

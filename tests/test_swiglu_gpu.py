@@ -97,17 +97,3 @@ def test_swiglu_rejects_odd_rows(nm):
     s = torch.cuda.current_stream().cuda_stream
     assert L.nm_spmv_swiglu(v.data_ptr(), m.data_ptr(), 3, 32, x.data_ptr(), h.data_ptr(), s) == 2
     assert L.nm_spmv_swiglu(v.data_ptr(), m.data_ptr(), 2, 32, x.data_ptr(), x.data_ptr(), s) == 7
-
-
-def test_swiglu_full_size_70b_gate_up(nm, orc):
-    rows, cols = 57344, 8192
-    W = synth.weights(rows, cols, 0, synth.stream_id(54, rows))
-    x = synth.activations(cols, 0, synth.stream_id(55, rows))
-    v, m = nm.nm_pack(to_dev(W), 2, 4)
-    got = from_dev(nm.nm_spmv_swiglu(v, m, to_dev(x)))
-    pairs = synth.sample_rows(rows // 2, 48, 0, synth.stream_id(56, rows))
-    rows_needed = np.sort(np.concatenate([2 * pairs, 2 * pairs + 1]))
-    ov, om = orc.prune_pack(np.ascontiguousarray(W[rows_needed]), 2, 4)
-    # in the sub-matrix, pair k sits at rows 2k, 2k+1
-    h, tol = reference(orc, ov, om, cols, x)
-    check(got[pairs], h, tol, "70B gate+up")
