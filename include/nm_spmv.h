@@ -312,7 +312,13 @@ int nm_spmm_prefill_plan(int64_t rows, int64_t cols, int64_t T, int sms, int *va
 /* nm_wait_timeouts -- how many times a tensor-core kernel's bounded wait on
  * one of its own barriers gave up (each such wait ends after 2 s, after which
  * the kernel abandons its work, skips its stores and returns, rather than
- * hang).  Zero in every correct run; reset to zero when `reset` != 0.
+ * hang).  The first wait that gives up also sets an abort flag: every other
+ * pipeline wait then gives up at once (waits for the block's own copies in
+ * flight still complete), and tensor-core blocks launched while the flag is
+ * set return without doing anything, so their Y is left unwritten.  Zero in
+ * every correct run; `reset` != 0 resets the count to zero and clears the
+ * abort flag.  After a nonzero count, treat the outputs of the tensor-core
+ * calls since the last reset as undefined.
  * Host-synchronous (reads a device counter); negative nm_status on error. */
 int64_t nm_wait_timeouts(int reset);
 

@@ -87,11 +87,11 @@ int64_t gemv_steps(int64_t cols) { return (cols + 511) / 512; }
 // Measured on GB300 over the decode-layer shapes: the {20 warps, 3 steps in
 // flight, fp16 x} variant streams large matrices fastest; below ~134M weight
 // positions (where the launch's fixed start-up cost weighs more) the
-// {24 warps, 2 steps, fp32 x} variant is ahead, and below ~33M the
-// {28 warps, 1 step, fp32 x} one.
+// {24 warps, 2 steps, fp32 x} variant is ahead, and up to 4096x4096 (2^24)
+// the {28 warps, 1 step, fp32 x} one.
 int default_spmv_variant(int64_t rows = 0, int64_t cols = 0) {
   const int64_t n = rows * cols;
-  return n >= ((int64_t)1 << 27) ? 1 : (n >= ((int64_t)1 << 25) ? 0 : 6);
+  return n >= ((int64_t)1 << 27) ? 1 : (n > ((int64_t)1 << 24) ? 0 : 6);
 }
 
 // The dense baseline's fastest variant on every decode-layer shape measured.
@@ -146,9 +146,9 @@ int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid,
                    SpmmPlan* plan, SpmmParams* p) {
   DeviceInfo d;
   if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
-  // measured on GB300 (70B layer shapes): 20 warps x 2 steps up to batch 4,
-  // 16 warps x 2 steps at batch 5-8
-  if (variant < 0) variant = batch <= 4 ? 1 : 0;
+  // measured on GB300 (70B layer shapes): 20 warps x 2 steps with the x slot
+  // unpacked inside the PTX up to batch 4, 16 warps x 2 steps at batch 5-8
+  if (variant < 0) variant = batch <= 4 ? 7 : 0;
   if (variant >= spmm_variant_count()) return NM_ERR_SHAPE;
   const int nw = spmm_variant_warps(variant);
   const int xf = spmm_variant_xf(variant);

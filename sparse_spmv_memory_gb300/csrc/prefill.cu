@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // After a wait gave up (this launch or an earlier one not yet reset), the
+  // block does nothing: the decision is block-uniform, taken before any
+  // barrier, copy or tensor-memory allocation.
+  if (__syncthreads_or(threadIdx.x == 0 && wait_aborted())) return;
   const int64_t r0 = (int64_t)blockIdx.y * BM;
   const int64_t n0 = (int64_t)blockIdx.x * L::BN;
   // K split: this block multiplies the mask words w0 .. w0 + nk - 1 (stage
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   // nothing in the last 2 s worth waiting for.
   auto drain = [&](int last) {
     for (int kt = last; kt >= 0 && kt > nk - 1 - STAGES; --kt)
-      mbar_wait(full(kt), full_par(kt), wait_limit_ns);
+      mbar_wait(full(kt), full_par(kt), wait_limit_ns, false);
   };
 
   if (warp == 0) {
@@ -451,6 +455,11 @@ __global__ void __launch_bounds__(threads_for(DW), 1)
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
+    // Tensor memory is freed only after the MMAs that write it have completed:
+    // one more bounded (not abortable) wait on the final commit, which a
+    // normal run passed already.  An MMA issuer that stopped early committed
+    // what it issued, so the barrier still completes.
+    mbar_wait(accum, 0, wait_limit_ns, false);
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
@@ -721,7 +730,10 @@ cudaError_t read_wait_timeouts(unsigned long long* count, int reset) {
   cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(*count));
   if (e != cudaSuccess || !reset) return e;
   const unsigned long long zero = 0;
-  return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+  const unsigned int clear = 0;
+  e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_wait_abort, &clear, sizeof(clear));
+  return e;
 }
 
 }  // namespace nmk

@@ -15,7 +15,8 @@
 //  * the same two-chain bfind scan as nm_spmv (values 15..8 from the top bit,
 //    0..7 from the bit-reversed mask; exhausted chains read zero pad rows);
 //  * per nonzero either one mixed-precision fp16*fp16+fp32 FMA per token
-//    (XF 0: fp16 slots) or one fp16->fp32 convert of the weight and one
+//    (XF 0: fp16 slots; XF 3: the same with the slot split into 16-bit
+//    registers inside the PTX) or one fp16->fp32 convert of the weight and one
 //    packed fp32x2 FMA per two tokens (XF 1: fp32 slots, twice the shared
 //    memory, half the FMA instructions at batch 4-8);
 //  * rows split over blocks and row-steps over warps as in nm_spmv
@@ -188,6 +189,78 @@ __device__ __forceinline__ void decode_word_batch_f32s(uint32_t m, const uint32_
   }
 }
 
+// The x slot's BP fp16 values unpacked into 16-bit registers inside the PTX
+// (mov.b32 {lo, hi} names the halves of a 32-bit register, so the mixed
+// fp16*fp16+fp32 FMAs take them without separate extraction instructions).
+// XF 3: one 4/8/16-byte shared load per nonzero, as XF 0.
+template <int BP>
+__device__ __forceinline__ void fma_slot_u32(uint32_t addr, uint16_t w, float (&a)[BP]) {
+  if constexpr (BP == 2) {
+    asm volatile(
+        "{.reg .b32 r0; .reg .b16 x0, x1;\n\t"
+        "ld.shared.b32 r0, [%2];\n\t"
+        "mov.b32 {x0, x1}, r0;\n\t"
+        "fma.rn.f32.f16 %0, %3, x0, %0;\n\t"
+        "fma.rn.f32.f16 %1, %3, x1, %1;}"
+        : "+f"(a[0]), "+f"(a[1])
+        : "r"(addr), "h"(w));
+  } else if constexpr (BP == 4) {
+    asm volatile(
+        "{.reg .b32 r0, r1; .reg .b16 x0, x1, x2, x3;\n\t"
+        "ld.shared.v2.b32 {r0, r1}, [%4];\n\t"
+        "mov.b32 {x0, x1}, r0;\n\t"
+        "mov.b32 {x2, x3}, r1;\n\t"
+        "fma.rn.f32.f16 %0, %5, x0, %0;\n\t"
+        "fma.rn.f32.f16 %1, %5, x1, %1;\n\t"
+        "fma.rn.f32.f16 %2, %5, x2, %2;\n\t"
+        "fma.rn.f32.f16 %3, %5, x3, %3;}"
+        : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3])
+        : "r"(addr), "h"(w));
+  } else {
+    asm volatile(
+        "{.reg .b32 r0, r1, r2, r3; .reg .b16 x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
+        "ld.shared.v4.b32 {r0, r1, r2, r3}, [%8];\n\t"
+        "mov.b32 {x0, x1}, r0;\n\t"
+        "mov.b32 {x2, x3}, r1;\n\t"
+        "mov.b32 {x4, x5}, r2;\n\t"
+        "mov.b32 {x6, x7}, r3;\n\t"
+        "fma.rn.f32.f16 %0, %9, x0, %0;\n\t"
+        "fma.rn.f32.f16 %1, %9, x1, %1;\n\t"
+        "fma.rn.f32.f16 %2, %9, x2, %2;\n\t"
+        "fma.rn.f32.f16 %3, %9, x3, %3;\n\t"
+        "fma.rn.f32.f16 %4, %9, x4, %4;\n\t"
+        "fma.rn.f32.f16 %5, %9, x5, %5;\n\t"
+        "fma.rn.f32.f16 %6, %9, x6, %6;\n\t"
+        "fma.rn.f32.f16 %7, %9, x7, %7;}"
+        : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]),
+          "+f"(a[7])
+        : "r"(addr), "h"(w));
+  }
+}
+
+// XF 3 decode: as decode_word_batch, the x slot unpacked inside the PTX.
+template <int BP>
+__device__ __forceinline__ void decode_word_batch_u(uint32_t m, const uint32_t (&v)[8],
+                                                    uint32_t col_addr, uint32_t row_bytes,
+                                                    float (&a)[2][BP]) {
+  uint32_t mh = m;
+  uint32_t ml = bit_reverse(m);
+  const uint32_t top = col_addr + 31u * row_bytes;
+  const uint32_t neg_row = 0u - row_bytes;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t bh = msb_index(mh);
+    const uint32_t bl = msb_index(ml);
+    const uint32_t ah = col_addr + bh * row_bytes;  // ~0u -> pad row 0
+    const uint32_t al = top + bl * neg_row;         // ~0u -> pad row 33
+    mh ^= bit_at(bh);
+    ml ^= bit_at(bl);
+    const int kh = 15 - k, kl = k;
+    fma_slot_u32<BP>(ah, half_of(v[kh >> 1], kh & 1), a[1]);
+    fma_slot_u32<BP>(al, half_of(v[kl >> 1], kl & 1), a[0]);
+  }
+}
+
 template <int U>
 struct SpmmBatch {
   uint32_t m[U];
@@ -232,7 +305,8 @@ template <int NW, int U, int BP, int XF>
 __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) float smem[];
   const int P = p.pitch;
-  constexpr int kSlotWords = XF ? BP : BP / 2;          // 32-bit words per slot
+  constexpr bool kF32 = XF == 1 || XF == 2;             // fp32 slots
+  constexpr int kSlotWords = kF32 ? BP : BP / 2;        // 32-bit words per slot
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] fp16 (XF 0)
   float* tile_f = smem;                                 // [34][P][BP] fp32 (XF 1)
   float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
@@ -287,9 +361,9 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
     }
 #pragma unroll
     for (int b = 0; b < 32; ++b) {
-      const int jp = (XF && BP == 8) ? (((j >> 2) ^ ((wl >> 2) & 1)) << 2) | (j & 3) : j;
+      const int jp = (kF32 && BP == 8) ? (((j >> 2) ^ ((wl >> 2) & 1)) << 2) | (j & 3) : j;
       const int64_t at = ((int64_t)(1 + b) * P + wl) * BP + jp;
-      if (XF) {
+      if (kF32) {
         const float2 f = half2_bits_to_float2(h[b >> 1]);
         tile_f[at] = (b & 1) ? f.y : f.x;
       } else {
@@ -330,6 +404,8 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
         const uint32_t col_addr = tile_base + (uint32_t)(cc.t * 32 + lane) * (kSlotWords * 4u);
         if (XF == 1)
           decode_word_batch_f32<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a2);
+        else if (XF == 3)
+          decode_word_batch_u<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
         else if (XF == 2)
           decode_word_batch_f32s<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a);
         else
@@ -387,13 +463,18 @@ __global__ void __launch_bounds__(256) spmm_combine_kernel(const float* __restri
 }
 
 size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf) {
-  return (size_t)34 * pitch * bp * (xf ? 4 : 2) + 2 * (size_t)nw * bp * sizeof(float) +
+  return (size_t)34 * pitch * bp * ((xf == 1 || xf == 2) ? 4 : 2) +
+         2 * (size_t)nw * bp * sizeof(float) +
          4 * (size_t)nw * sizeof(int);
 }
 
 int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8); }
 
-// (warps per block, steps in flight per warp, x slot format)
+// (warps per block, steps in flight per warp, x slot format).  At batch 8
+// the kernel is issue-bound: 8 FMAs per nonzero per lane put a warp-step at
+// ~300 instructions (ncu, 70B gate+up: issue 78 % busy, shared-memory pipe
+// 87 % busy from the 16-byte x gather per nonzero), so it streams weights at
+// ~55 % of the HBM rate there; XF 3 gains 1-2 % at batch 4 only.
 // fp32 slots (XF 1: packed fp32x2 FMA; XF 2: scalar FMA) measured 1.5-1.7x
 // slower than fp16 slots at batch 4-8 on GB300: every nonzero gathers
 // BP x-values from shared memory per lane, so at batch 8 the gather already
@@ -401,7 +482,8 @@ int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8);
 // shared-memory bandwidth, not FMA issue, is the limit there.  They stay
 // available for tuning; the defaults use fp16 slots.
 static const int kSpmmVariants[][3] = {{16, 2, 0}, {20, 2, 0}, {12, 3, 0}, {24, 1, 0},
-                                       {16, 2, 1}, {16, 2, 2}};
+                                       {16, 2, 1}, {16, 2, 2}, {16, 2, 3}, {20, 2, 3},
+                                       {24, 1, 3}, {12, 3, 3}};
 
 int spmm_variant_count() { return (int)(sizeof(kSpmmVariants) / sizeof(kSpmmVariants[0])); }
 
@@ -449,7 +531,7 @@ cudaError_t launch_spmm(const SpmmParams& p0, const SpmmPlan& plan, int flags,
         p, plan.bp, plan.grid, flags, stream);                                          \
     break;
     NM_SPMM_CASE(0) NM_SPMM_CASE(1) NM_SPMM_CASE(2) NM_SPMM_CASE(3) NM_SPMM_CASE(4)
-    NM_SPMM_CASE(5)
+    NM_SPMM_CASE(5) NM_SPMM_CASE(6) NM_SPMM_CASE(7) NM_SPMM_CASE(8) NM_SPMM_CASE(9)
 #undef NM_SPMM_CASE
     default: return cudaErrorInvalidValue;
   }

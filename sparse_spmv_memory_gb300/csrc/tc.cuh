@@ -12,6 +12,17 @@ namespace nmk {
 // translation unit (prefill.cu) includes this header.
 __device__ unsigned long long g_wait_timeouts = 0;
 
+// Set by the first wait that gives up; every later abortable wait (in any
+// block, and in later launches until nm_wait_timeouts(1) clears it) gives up
+// at once, and new blocks return before allocating anything, so one lost
+// arrival ends the whole launch after one wait limit instead of one limit per
+// wait per block.
+__device__ unsigned int g_wait_abort = 0;
+
+__device__ __forceinline__ bool wait_aborted() {
+  return *(volatile unsigned int*)&g_wait_abort != 0u;
+}
+
 // A wait gives up after this long (ns of %globaltimer): far above any
 // legitimate wait inside one block, short enough that a lost arrival ends
 // the kernel instead of hanging the GPU.
@@ -59,16 +70,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the barrier's phase with the given parity has completed.
-// Returns false (and counts a timeout) if that takes longer than limit_ns;
-// the caller then abandons its loop and goes to teardown.
+// Returns false (and counts a timeout) if that takes longer than limit_ns, or
+// at once once another wait has given up (abortable waits only); the caller
+// then abandons its loop and goes to teardown.  A drain of the block's own
+// copies in flight is not abortable: those copies land whatever else failed,
+// and shared memory must not be released under them.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+                                          uint64_t limit_ns = kWaitLimitNs,
+                                          bool abortable = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((int64_t)(global_timer_ns() - t0) > (int64_t)limit_ns) {  // a step back is no timeout
+    const bool abort = abortable && wait_aborted();
+    if (abort || (int64_t)(global_timer_ns() - t0) > (int64_t)limit_ns) {  // a step back is no timeout
       atomicAdd(&g_wait_timeouts, 1ull);
+      atomicExch(&g_wait_abort, 1u);
       return false;
     }
   }

@@ -383,7 +383,9 @@ def test_bounded_waits_end_a_stalled_prefill_kernel(nm, orc):
     elapsed = time.time() - t0
     assert nm.nm_wait_timeouts(reset=True) > 0
     assert bool((Y == 3.0).all())
-    assert elapsed < 30.0
+    # the first wait to give up aborts every other one: the launch ends after
+    # about one wait limit (20 ms), not one per wait and block
+    assert elapsed < 2.0
     Y2 = f16_to_f64(from_dev(nm.nm_spmm_prefill(v, m, Xd)))
     torch.cuda.synchronize()
     y_ref, s = oracle_Y(orc, ov, om, cols, X)
