@@ -254,7 +254,7 @@ int64_t nm_spmv_max_cols(void) {
     nw = w > nw ? w : nw;
   }
   // largest multiple-of-32 pitch whose tile fits, times 32 columns per word
-  int64_t pitch = ((int64_t)d.smem_optin / 4 - 2 * nw) / 34;
+  int64_t pitch = ((int64_t)d.smem_optin / 4 - 6 * nw) / 34;
   pitch = pitch / 32 * 32;
   return pitch * 32;
 }
