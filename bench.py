@@ -606,71 +606,73 @@ def run_gpu(args):
     results = {}
     per_launch = None
     cs = ClockSampler(local).__enter__()
-    for pat in patterns:
-        slots = pack_slots(nm, dense, pat, args.slots)
-        fn = lambda: step.run_sparse(slots)
-        if pat == head:
-            per, total = time_graph(fn, args.steps, args.warmup, stream, clock=cs)
-            per_launch = time_per_matrix(step, slots, stream, 10)
-        else:
-            per, total = time_graph(fn, max(3, args.steps // 4), max(3, args.warmup), stream,
-                                    clock=cs)
-        results[pat] = (per, total, len(per))
-        del slots, fn
+    try:
+        for pat in patterns:
+            slots = pack_slots(nm, dense, pat, args.slots)
+            fn = lambda: step.run_sparse(slots)
+            if pat == head:
+                per, total = time_graph(fn, args.steps, args.warmup, stream, clock=cs)
+                per_launch = time_per_matrix(step, slots, stream, 10)
+            else:
+                per, total = time_graph(fn, max(3, args.steps // 4), max(3, args.warmup), stream,
+                                        clock=cs)
+            results[pat] = (per, total, len(per))
+            del slots, fn
+            torch.cuda.empty_cache()
+
+        # end to end through the public calls: pinned host x in, y out, every step
+        slots = pack_slots(nm, dense, head, args.slots)
+        x_host = torch.empty(step.x_all.shape, dtype=torch.float16, pin_memory=True)
+        x_host.copy_(step.x_all)
+        y_host = torch.empty(step.y_all.shape, dtype=torch.float16, pin_memory=True)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step.x_all.copy_(x_host, non_blocking=True)
+                step.run_sparse(slots)
+                y_host.copy_(step.y_all, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                step.x_all.copy_(x_host, non_blocking=True)
+                step.run_sparse(slots)
+                y_host.copy_(step.y_all, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_wall = time.perf_counter() - t0
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        barrier()
+        del slots
         torch.cuda.empty_cache()
 
-    # end to end through the public calls: pinned host x in, y out, every step
-    slots = pack_slots(nm, dense, head, args.slots)
-    x_host = torch.empty(step.x_all.shape, dtype=torch.float16, pin_memory=True)
-    x_host.copy_(step.x_all)
-    y_host = torch.empty(step.y_all.shape, dtype=torch.float16, pin_memory=True)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step.x_all.copy_(x_host, non_blocking=True)
-            step.run_sparse(slots)
-            y_host.copy_(step.y_all, non_blocking=True)
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            step.x_all.copy_(x_host, non_blocking=True)
-            step.run_sparse(slots)
-            y_host.copy_(step.y_all, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_wall = time.perf_counter() - t0
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    barrier()
-    del slots
-    torch.cuda.empty_cache()
-
-    # dense baselines on the same shapes and rotation scheme: the library's own
-    # dense_gemv, and cuBLAS as the sanity line (batch one)
-    dense_res = cublas_ms = None
-    if args.dense:
-        dslots = dense_slots(dense, args.dense_slots)
-        dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
-                                  args.warmup, stream, clock=cs)
-        dense_res = (dper, dtotal, len(dper))
-        if args.batch == 1:
-            cper, ctotal = time_graph(lambda: step.run_cublas(dslots), max(3, args.steps // 2),
+        # dense baselines on the same shapes and rotation scheme: the library's own
+        # dense_gemv, and cuBLAS as the sanity line (batch one)
+        dense_res = cublas_ms = None
+        if args.dense:
+            dslots = dense_slots(dense, args.dense_slots)
+            dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
                                       args.warmup, stream, clock=cs)
-            cublas_ms = ctotal / len(cper) * 1e3
-        del dslots
+            dense_res = (dper, dtotal, len(dper))
+            if args.batch == 1:
+                cper, ctotal = time_graph(lambda: step.run_cublas(dslots), max(3, args.steps // 2),
+                                          args.warmup, stream, clock=cs)
+                cublas_ms = ctotal / len(cper) * 1e3
+            del dslots
+            torch.cuda.empty_cache()
+        del dense
         torch.cuda.empty_cache()
-    del dense
-    torch.cuda.empty_cache()
 
-    # the other decode-layer workloads, batch one, on the same line
-    side = {}
-    if args.side and args.batch == 1 and not args.swiglu:
-        for wname in WORKLOADS:
-            if wname != args.workload:
-                side[wname] = measure_side(nm, wname, device, stream, args, peak, cs)
-    cs.__exit__(None, None, None)
+        # the other decode-layer workloads, batch one, on the same line
+        side = {}
+        if args.side and args.batch == 1 and not args.swiglu:
+            for wname in WORKLOADS:
+                if wname != args.workload:
+                    side[wname] = measure_side(nm, wname, device, stream, args, peak, cs)
+    finally:
+        cs.__exit__(None, None, None)
     clocks = cs.summary()
 
     # ---- assemble ------------------------------------------------------------
