@@ -301,41 +301,16 @@ __device__ __forceinline__ void spmm_load(SpmmBatch<U>& bt, SpmmCursor& c, int64
   }
 }
 
-template <int NW, int U, int BP, int XF>
-__global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
-  extern __shared__ __align__(16) float smem[];
-  const int P = p.pitch;
-  constexpr bool kF32 = XF == 1 || XF == 2;             // fp32 slots
-  constexpr int kSlotWords = kF32 ? BP : BP / 2;        // 32-bit words per slot
-  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] fp16 (XF 0)
-  float* tile_f = smem;                                 // [34][P][BP] fp32 (XF 1)
-  float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
-  float* pl = pf + NW * BP;                             // [NW][BP]
-  int* rinfo = reinterpret_cast<int*>(pl + NW * BP);    // [NW][4]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sl = (int)(blockIdx.x / (unsigned)p.bps), c = blockIdx.x - sl * p.bps;  // slice, block in it
-  const BlockRows br = split_part(c, p.rows_q, p.rows_r, p.bps);
-  const int64_t r0 = br.r0, r1 = br.r1;
-  const BlockRows sr = split_part(sl, p.steps_q, p.steps_r, p.slices);
-  const int ts0 = (int)sr.r0, ts1 = (int)sr.r1;
-  const int T = ts1 - ts0;              // warp-steps per row in this slice
-  const int w0 = ts0 * 32;              // first mask word of the slice
-  const int wend = min(ts1 * 32, p.words);
-  const int64_t F = (r1 - r0) * T;
-  const WarpRange wr = warp_range<NW>(F, warp);
-  const int64_t row0 = div_steps(wr.sb, T);
-  const int t0 = (int)(wr.sb - row0 * T);
-
-  SpmmCursor lc{wr.sb, row0, t0};
-  SpmmBatch<U> A, B;
-  pdl_launch_dependents();
-  if (!p.early_weights) pdl_wait_previous();
-  spmm_load<U>(A, lc, wr.se, T, p, r0, w0, wend, lane);
-  if (p.early_weights) pdl_wait_previous();  // X (and Y, the workspace) may be the previous kernel's
-
-  // Stage the slice of X: tile[1 + b][wl][j] = X[j][32 (w0 + wl) + b].
-  const int nthreads = NW * 32;
+// Stage one column slice of X in shared memory: tile[1 + b][wl][j] =
+// X[j][32 (w0 + wl) + b] for the slice's words w0 + wl < wend (fp16, or fp32
+// with the two 16-byte halves of a 32-byte slot swapped for odd word groups),
+// zero pad rows 0 and 33, tokens past the batch zero.
+template <int BP, bool F32>
+__device__ __forceinline__ void stage_x_slice(float* smem, const SpmmParams& p, int P, int w0,
+                                              int wend, int nthreads) {
+  constexpr int kSlotWords = F32 ? BP : BP / 2;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
+  float* tile_f = smem;
   uint32_t* tile32 = reinterpret_cast<uint32_t*>(smem);
   for (int i = threadIdx.x; i < P * kSlotWords; i += nthreads) {
     tile32[i] = 0u;
@@ -361,9 +336,9 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
     }
 #pragma unroll
     for (int b = 0; b < 32; ++b) {
-      const int jp = (kF32 && BP == 8) ? (((j >> 2) ^ ((wl >> 2) & 1)) << 2) | (j & 3) : j;
+      const int jp = (F32 && BP == 8) ? (((j >> 2) ^ ((wl >> 2) & 1)) << 2) | (j & 3) : j;
       const int64_t at = ((int64_t)(1 + b) * P + wl) * BP + jp;
-      if (kF32) {
+      if (F32) {
         const float2 f = half2_bits_to_float2(h[b >> 1]);
         tile_f[at] = (b & 1) ? f.y : f.x;
       } else {
@@ -371,6 +346,66 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
       }
     }
   }
+}
+
+// Warp sums of BP per-lane values (one per token) in five xor levels: first
+// log2(BP) split levels (xor 16, 8, ...) where each lane keeps half of its
+// remaining values and adds its partner's copy of that half, then plain
+// butterfly levels on the one value left.  Lane L ends with the total of
+// token L / (32 / BP) -- BP - 1 + log2(32 / BP) shuffles instead of 5 BP,
+// and every total is bit for bit that of a butterfly per token (each level
+// adds the same two partial sums, and fp32 addition commutes).
+template <int BP>
+__device__ __forceinline__ float warp_sum_tokens(float (&v)[BP], int lane) {
+#pragma unroll
+  for (int half = BP / 2, off = 16; half >= 1; half /= 2, off /= 2) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = up ? v[i] : v[half + i];
+      const float keep = up ? v[half + i] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int off = 16 / BP; off > 0; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+  return t;
+}
+
+template <int NW, int U, int BP, int XF>
+__global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
+  extern __shared__ __align__(16) float smem[];
+  const int P = p.pitch;
+  constexpr bool kF32 = XF == 1 || XF == 2;             // fp32 slots
+  constexpr int kSlotWords = kF32 ? BP : BP / 2;        // 32-bit words per slot
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);   // [34][P][BP] slots
+  float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
+  float* pl = pf + NW * BP;                             // [NW][BP]
+  int* rinfo = reinterpret_cast<int*>(pl + NW * BP);    // [NW][4]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sl = (int)(blockIdx.x / (unsigned)p.bps), c = blockIdx.x - sl * p.bps;  // slice, block in it
+  const BlockRows br = split_part(c, p.rows_q, p.rows_r, p.bps);
+  const int64_t r0 = br.r0, r1 = br.r1;
+  const BlockRows sr = split_part(sl, p.steps_q, p.steps_r, p.slices);
+  const int ts0 = (int)sr.r0, ts1 = (int)sr.r1;
+  const int T = ts1 - ts0;              // warp-steps per row in this slice
+  const int w0 = ts0 * 32;              // first mask word of the slice
+  const int wend = min(ts1 * 32, p.words);
+  const int64_t F = (r1 - r0) * T;
+  const WarpRange wr = warp_range<NW>(F, warp);
+  const int64_t row0 = div_steps(wr.sb, T);
+  const int t0 = (int)(wr.sb - row0 * T);
+
+  SpmmCursor lc{wr.sb, row0, t0};
+  SpmmBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
+  spmm_load<U>(A, lc, wr.se, T, p, r0, w0, wend, lane);
+  if (p.early_weights) pdl_wait_previous();  // X (and Y, the workspace) may be the previous kernel's
+
+  stage_x_slice<BP, kF32>(smem, p, P, w0, wend, NW * 32);
   __syncthreads();
 
   const uint32_t row_bytes = (uint32_t)P * kSlotWords * 4u;
@@ -446,6 +481,168 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
   combine_cut_rows_n<NW, BP>(rinfo, pf, pl, store);
 }
 
+// Whole-step kernel (cols % 1024 == 0, so every step of every slice is 32
+// whole mask words): as spmm_kernel, but a warp's steps are walked by pointer
+// increments with no per-step predication (as in spmv_full_kernel) -- one
+// contiguous stretch per row slice, a fixed jump over the other slices' steps
+// at each row change -- and a row's BP sums are reduced by warp_sum_tokens,
+// each token's total then held (and stored) by its own lane.  SLICED is
+// false for a single column slice: the block's steps are then one contiguous
+// stretch and the sums go straight to Y, with no slice bookkeeping at all
+// (it cost 2-5 % at 2-4 tokens when kept as run-time checks).
+template <int U, bool SLICED>
+__device__ __forceinline__ void load_steps_batch(SpmmBatch<U>& bt, const uint32_t*& vp,
+                                                 const uint32_t*& mp, int& lt, int Ts,
+                                                 int skip) {
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    bt.m[i] = ld_stream_u32(mp);
+    ld_stream_v8(vp, bt.v[i]);
+    mp += 32;
+    vp += 256;
+    if (SLICED && ++lt == Ts) {  // next row: jump over the other slices' steps
+      lt = 0;
+      mp += 32 * skip;
+      vp += 256 * skip;
+    }
+  }
+}
+
+template <int NW, int U, int BP, int XF, bool SLICED>
+__global__ void __launch_bounds__(NW * 32, 1) spmm_full_kernel(const SpmmParams p) {
+  extern __shared__ __align__(16) float smem[];
+  const int P = p.pitch;
+  constexpr bool kF32 = XF == 1 || XF == 2;
+  constexpr int kSlotWords = kF32 ? BP : BP / 2;
+  constexpr int kLanesPerToken = 32 / BP;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
+  float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
+  float* pl = pf + NW * BP;                             // [NW][BP]
+  int* rinfo = reinterpret_cast<int*>(pl + NW * BP);    // [NW][4]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int sl = 0, ts0 = 0, Ts = p.steps;  // slice, its first step and steps of a row
+  BlockRows br;
+  if (SLICED) {
+    sl = (int)(blockIdx.x / (unsigned)p.bps);
+    const int c = blockIdx.x - sl * p.bps;  // block within the slice
+    br = split_part(c, p.rows_q, p.rows_r, p.bps);
+    const BlockRows sr = split_part(sl, p.steps_q, p.steps_r, p.slices);
+    ts0 = (int)sr.r0;
+    Ts = (int)(sr.r1 - sr.r0);
+  } else {
+    br = block_rows(p.rows_q, p.rows_r);
+  }
+  const int skip = p.steps - Ts;  // the other slices' steps
+  const int F = (int)((br.r1 - br.r0) * Ts);
+  const WarpRange wr = warp_range<NW>(F, warp);
+  const int sb = (int)wr.sb, se = (int)wr.se;
+  const int nfull = (se - sb) / U;
+
+  const int row0 = sb / Ts, t0 = sb - row0 * Ts;
+  const int64_t g = (br.r0 + row0) * (int64_t)p.steps + ts0 + t0;  // first step, global
+  const uint32_t* mp = p.masks + g * 32 + lane;
+  const uint32_t* vp = p.values + (g * 32 + lane) * 8;
+  int lt = t0;
+
+  SpmmBatch<U> A, B;
+  pdl_launch_dependents();
+  if (!p.early_weights) pdl_wait_previous();
+  if (nfull > 0) load_steps_batch<U, SLICED>(A, vp, mp, lt, Ts, skip);
+  if (p.early_weights) pdl_wait_previous();  // X (and Y, the workspace) may be the previous kernel's
+  stage_x_slice<BP, kF32>(smem, p, P, ts0 * 32, (ts0 + Ts) * 32, NW * 32);
+  __syncthreads();
+
+  const uint32_t row_bytes = (uint32_t)P * kSlotWords * 4u;
+  const uint32_t swz = ((lane >> 2) & 1) ? 16u : 0u;  // local word bit 2 == lane bit 2
+  const uint32_t lane_col = smem_addr(tile) + row_bytes + (uint32_t)lane * (kSlotWords * 4u);
+  constexpr uint32_t kStepBytes = 32u * kSlotWords * 4u;  // 32 words of slots
+  // one token's sum of local row `row`: Y, or this slice's fp32 partial
+  auto put = [&](int row, int j, float v) {
+    const int64_t gr = br.r0 + row;
+    if (!SLICED)
+      p.Y[(int64_t)j * p.ldy + gr] = __float2half_rn(v);
+    else
+      p.partial[((int64_t)sl * p.batch + j) * p.rows + gr] = v;
+  };
+  auto store = [&](int row, const float (&v)[BP]) {  // the cut-row combine: all tokens
+#pragma unroll
+    for (int j = 0; j < BP; ++j)
+      if (j < p.batch) put(row, j, v[j]);
+  };
+
+  int row = row0, t = t0;
+  uint32_t col_addr = lane_col + kStepBytes * (uint32_t)t;
+  float a[2][BP];                    // XF 0, 2, 3
+  unsigned long long a2[2][BP / 2];  // XF 1: packed pairs of tokens
+#pragma unroll
+  for (int j = 0; j < BP; ++j) a[0][j] = a[1][j] = 0.f;
+#pragma unroll
+  for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
+
+  // A row's sums: reduced across the warp, each token's total on its own
+  // lane, which stores it (whole row) or keeps it as a cut-row partial.
+  auto finish = [&](bool whole) {
+    float v[BP];
+#pragma unroll
+    for (int j = 0; j < BP; ++j) {
+      v[j] = XF == 1 ? ((j & 1) ? pair_hi(a2[0][j >> 1]) + pair_hi(a2[1][j >> 1])
+                                : pair_lo(a2[0][j >> 1]) + pair_lo(a2[1][j >> 1]))
+                     : a[0][j] + a[1][j];
+      a[0][j] = a[1][j] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
+    const float total = warp_sum_tokens<BP>(v, lane);
+    if (lane % kLanesPerToken == 0) {
+      const int j = lane / kLanesPerToken;
+      if (whole) {
+        if (j < p.batch) put(row, j, total);
+      } else {
+        ((row == row0) ? pf : pl)[warp * BP + j] = total;
+      }
+    }
+  };
+
+  auto step = [&](uint32_t m, const uint32_t (&v)[8]) {
+    if (XF == 1)
+      decode_word_batch_f32<BP>(m, v, col_addr, row_bytes, swz, a2);
+    else if (XF == 3)
+      decode_word_batch_u<BP>(m, v, col_addr, row_bytes, a);
+    else if (XF == 2)
+      decode_word_batch_f32s<BP>(m, v, col_addr, row_bytes, swz, a);
+    else
+      decode_word_batch<BP>(m, v, col_addr, row_bytes, a);
+    col_addr += kStepBytes;
+    if (++t == Ts) {  // the row's slice complete
+      finish(row != row0 || t0 == 0);
+      t = 0;
+      ++row;
+      col_addr = lane_col;
+    }
+  };
+
+  for (int i = 0; i < nfull; i += 2) {
+    if (i + 1 < nfull) load_steps_batch<U, SLICED>(B, vp, mp, lt, Ts, skip);
+#pragma unroll
+    for (int u = 0; u < U; ++u) step(A.m[u], A.v[u]);
+    if (i + 1 >= nfull) break;
+    if (i + 2 < nfull) load_steps_batch<U, SLICED>(A, vp, mp, lt, Ts, skip);
+#pragma unroll
+    for (int u = 0; u < U; ++u) step(B.m[u], B.v[u]);
+  }
+  for (int s = sb + nfull * U; s < se; ++s) {
+    SpmmBatch<1> one;
+    load_steps_batch<1, SLICED>(one, vp, mp, lt, Ts, skip);
+    step(one.m[0], one.v[0]);
+  }
+  if (se > sb && t != 0) finish(false);  // the warp's range ends inside a row
+  note_range(rinfo, warp, lane, se > sb ? row0 : -1, t0 != 0, t != 0 ? row : row - 1, t != 0);
+
+  __syncthreads();
+  combine_cut_rows_n<NW, BP>(rinfo, pf, pl, store);
+}
+
 // Y[j][r] = sum over slices s (in order) of partial[s][j][r], rounded to fp16.
 __global__ void __launch_bounds__(256) spmm_combine_kernel(const float* __restrict__ partial,
                                                            int slices, int batch, int64_t rows,
@@ -472,9 +669,12 @@ int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8);
 
 // (warps per block, steps in flight per warp, x slot format).  At batch 8
 // the kernel is issue-bound: 8 FMAs per nonzero per lane put a warp-step at
-// ~300 instructions (ncu, 70B gate+up: issue 78 % busy, shared-memory pipe
-// 87 % busy from the 16-byte x gather per nonzero), so it streams weights at
-// ~55 % of the HBM rate there; XF 3 gains 1-2 % at batch 4 only.
+// ~300 instructions (ncu, 70B gate+up, general kernel: issue 78 % busy,
+// shared-memory pipe 87 % busy from the 16-byte x gather per nonzero); the
+// whole-step kernel's unpredicated walk and split-level token reduction
+// raise it from ~55 % to ~61 % of the HBM rate there.  XF 3 helped the
+// general kernel by 1-2 % at batch 4 only and is slower in the whole-step
+// kernel.
 // fp32 slots (XF 1: packed fp32x2 FMA; XF 2: scalar FMA) measured 1.5-1.7x
 // slower than fp16 slots at batch 4-8 on GB300: every nonzero gathers
 // BP x-values from shared memory per lane, so at batch 8 the gather already
@@ -497,11 +697,21 @@ int spmm_variant_xf(int variant) {
 
 template <int NW, int U, int BP, int XF>
 static cudaError_t launch_spmm_t(const SpmmParams& p, int grid, int flags, cudaStream_t stream) {
-  static int smem_set[64] = {0};
+  static int smem_set[64] = {0}, smem_full[64] = {0}, smem_sliced[64] = {0};
+  const size_t smem = spmm_smem_bytes(p.pitch, NW, BP, XF);
+  const int64_t block_steps = (p.rows_q + 2) * (int64_t)p.steps;
+  if (p.words % 32 == 0 && block_steps < (int64_t)0x7FFFFFFF) {
+    auto* k = p.slices == 1 ? spmm_full_kernel<NW, U, BP, XF, false>
+                            : spmm_full_kernel<NW, U, BP, XF, true>;
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k),
+                                    p.slices == 1 ? smem_full : smem_sliced, 64);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
+  }
   auto* k = spmm_kernel<NW, U, BP, XF>;
   cudaError_t e = ensure_max_smem(reinterpret_cast<const void*>(k), smem_set, 64);
   if (e != cudaSuccess) return e;
-  return launch_kernel(k, grid, NW * 32, spmm_smem_bytes(p.pitch, NW, BP, XF), stream, flags, p);
+  return launch_kernel(k, grid, NW * 32, smem, stream, flags, p);
 }
 
 template <int NW, int U, int XF>

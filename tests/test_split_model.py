@@ -205,3 +205,42 @@ def test_spmm_slices_cover_every_step_once(rows, T):
                     writes[(r, sl)] = writes.get((r, sl), 0) + 1
             assert len(reads) == rows * T and all(v == 1 for v in reads.values())
             assert len(writes) == rows * S and all(v == 1 for v in writes.values())
+
+
+@pytest.mark.parametrize("rows,T", [(1, 1), (7, 3), (300, 8), (57, 28), (4096, 4), (33, 14)])
+def test_sliced_whole_step_loads_walk_each_rows_slice(rows, T):
+    """The whole-step small-batch kernel walks each warp's loads by pointer
+    increments: +1 step per step and, when a row's slice is done, a jump over
+    the other slices' steps.  Model that walk (steps counted from the matrix
+    start, as the masks pointer moves in units of one step's 32 words) and
+    check it visits exactly the (row, step) pairs of the warp's range, in
+    order, for every slice split of every launch size; and that the loads
+    issued ahead in batches of U never run past the range's last step."""
+    for S in sorted({1, 2, 3, T}):
+        if S > T:
+            continue
+        for grid, NW, U in [(1, 16, 2), (7, 20, 2), (152, 20, 3), (152, 16, 2), (3, 24, 1)]:
+            bps = max(1, min(grid // S, rows))
+            for b in range(bps * S):
+                sl, c = divmod(b, bps)
+                r0, r1 = split_part(c, rows, bps)
+                ts0, ts1 = split_part(sl, T, S)
+                Ts, skip = ts1 - ts0, T - (ts1 - ts0)
+                F = (r1 - r0) * Ts
+                for w in range(NW):
+                    sb, se = warp_range(F, NW, w)
+                    if se <= sb:
+                        continue
+                    row0, t0 = divmod(sb, Ts)
+                    ptr, lt = (r0 + row0) * T + ts0 + t0, t0
+                    seen = []
+                    nfull = (se - sb) // U
+                    loads = nfull * U + (se - sb - nfull * U)
+                    for _ in range(loads):
+                        seen.append(ptr)
+                        ptr += 1
+                        lt += 1
+                        if lt == Ts:
+                            lt, ptr = 0, ptr + skip
+                    want = [(r0 + s // Ts) * T + ts0 + s % Ts for s in range(sb, se)]
+                    assert seen == want, (rows, T, S, grid, NW, U, b, w)
