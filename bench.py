@@ -254,8 +254,16 @@ def ncu_traffic(shape_key: str, record="nm_spmv_traffic.json", sources=None):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_pack_sample(mats, pattern, rows_per):
-    """Oracle-packed first ``rows_per`` rows of every matrix (not timed)."""
+def batch_metric(batch: int) -> str:
+    """The line's metric: the headline's at one token, the SpMM's at 2..8."""
+    if batch == 1:
+        return METRIC
+    return f"N:M SpMM at {batch} tokens: achieved HBM GB/s (% peak); speedup vs cuBLAS"
+
+
+def oracle_pack_sample(mats, pattern, rows_per, tokens=1):
+    """Oracle-packed first ``rows_per`` rows of every matrix and ``tokens``
+    activation vectors per matrix (not timed)."""
     import oracle
     import synth
     orc = oracle.Oracle()
@@ -264,17 +272,20 @@ def oracle_pack_sample(mats, pattern, rows_per):
     for mi, (name, rows, cols) in enumerate(mats):
         n = min(rows_per, rows)
         W = synth.normal_f16((n, cols), 0, synth.stream_id(2, mi, 0), synth.WEIGHT_SIGMA)
-        x = synth.activations(cols, 0, synth.stream_id(2, mi, 1))
+        xs = [synth.activations(cols, 0, synth.stream_id(2, mi, 1) if t == 0
+                                else synth.stream_id(2, mi, 1, t)) for t in range(tokens)]
         v, m = orc.prune_pack(W, N, M)
-        packed.append((v, m, cols, x, n))
+        packed.append((v, m, cols, xs, n))
     return orc, packed
 
 
 def oracle_run(orc, packed):
-    """The timed oracle work: unpack to dense + double matvec; returns bytes."""
+    """The timed oracle work: unpack to dense + double matvec per token;
+    returns the weight bytes (counted once per step, whatever the tokens)."""
     nbytes = 0
-    for v, m, cols, x, n in packed:
-        orc.spmv_f64(v, m, cols, x)
+    for v, m, cols, xs, n in packed:
+        for x in xs:
+            orc.spmv_f64(v, m, cols, x)
         nbytes += sparse_bytes(n, cols)
     return nbytes
 
@@ -508,11 +519,18 @@ SIDE_PATTERNS = {"single_4096": [(2, 4)], "llama31_8b_layer": [(2, 4)],
                  "llama33_70b_layer": PATTERNS}
 
 
-def spmv_kernel_label(nm, rows, cols):
-    """Which kernel and plan the library runs for one nm_spmv call."""
+def spmv_kernel_label(nm, rows, cols, batch=1):
+    """Which kernel and plan the library runs for one nm_spmv (batch one) or
+    nm_spmm (2..8 tokens) call."""
+    if batch > 1:
+        ws = nm.nm_spmm_workspace_bytes(rows, cols, batch)
+        slices = ws // (batch * rows * 4) if ws else 1
+        kern = "spmm_full_kernel" if cols % 1024 == 0 else "spmm_kernel"
+        return (f"nm_spmm: {kern} (default plan, {slices} column slice"
+                f"{'s + spmm_combine_kernel' if slices > 1 else ''})")
     v, g, w = nm.nm_spmv_plan(rows, cols)
     kern = "spmv_full_kernel" if cols % 1024 == 0 else "spmv_kernel"
-    return f"{kern} (nm_spmv plan: variant {v}, {w} warps x {g} blocks)"
+    return f"nm_spmv: {kern} (nm_spmv plan: variant {v}, {w} warps x {g} blocks)"
 
 
 def time_dense_lines(step, dslots, stream, args, clock):
@@ -682,7 +700,7 @@ def run_gpu(args):
     gbs = units / secs / 1e9
     med_ms = statistics.median(per)
     out = {
-        "metric": METRIC,
+        "metric": batch_metric(args.batch),
         "value": round(gbs, 1),
         "unit": "GB/s",
         "n_gpus": world,
@@ -704,7 +722,8 @@ def run_gpu(args):
                           f"{args.slots * step_bytes / layers / 1e9:.1f} GB > L2 (129 MB)"),
             "parallelism": f"replicas x{world}",
             "launch_flags": "library default (programmatic dependent launch)" if args.flags < 0 else args.flags,
-            "gate_up": "nm_spmv_swiglu (SwiGLU fused)" if args.swiglu and args.batch == 1 else "nm_spmv",
+            "gate_up": ("nm_spmv_swiglu (SwiGLU fused)" if args.swiglu and args.batch == 1
+                        else ("nm_spmv" if args.batch == 1 else "nm_spmm")),
         },
         "step_ms": {"median": round(med_ms, 4), "p10": round(float(np.percentile(per, 10)), 4),
                     "p90": round(float(np.percentile(per, 90)), 4)},
@@ -734,7 +753,7 @@ def run_gpu(args):
     achieved = dom_bytes / dom_us / 1e3
     traffic = ncu_traffic(f"{dom[1]}x{dom[2]}")
     out["roofline"] = {
-        "bound": "hbm", "kernel": "nm_spmv: " + spmv_kernel_label(nm, dom[1], dom[2]),
+        "bound": "hbm", "kernel": spmv_kernel_label(nm, dom[1], dom[2], args.batch),
         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4),
         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -771,7 +790,8 @@ def run_gpu(args):
             out["speedup_vs_cublas"] = round(cublas_ms / (total / k * 1e3), 4)
         out["speedup_vs_dense"] = round(best / (total / k * 1e3), 4)
         out["speedup_vs_dense_basis"] = ("the faster of dense_gemv and cuBLAS"
-                                         if cublas_ms is not None else "dense_gemv")
+                                         if cublas_ms is not None else
+                                         ("dense_gemv" if args.batch == 1 else "cuBLAS (torch.mm)"))
         out["speedup_ideal"] = round(step.bytes_dense() / step_bytes, 4)
         for p in patterns:
             out["patterns"][f"{p[0]}:{p[1]}"]["speedup_vs_dense"] = round(
@@ -785,7 +805,8 @@ def run_gpu(args):
                   "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
                   "ms_per_step": round(e_secs / args.steps * 1e3, 4),
                   "host_wall_ms_per_step": round(e2e_wall / args.steps * 1e3, 4),
-                  "path": "Python binding -> C ABI nm_spmv per call, eager, pinned host x/y"}
+                  "path": (f"Python binding -> C ABI {'nm_spmv' if args.batch == 1 else 'nm_spmm'} "
+                           "per call, eager, pinned host x/y")}
     out["clocks"] = clocks
     out["setup_s"] = round(setup_s, 1)
 
@@ -1010,8 +1031,11 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0},
         }
     per_step = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
-    rows_per, _, _, desc = oracle_sample(mats, head, per_step)
-    orc, packed = oracle_pack_sample(mats, head, rows_per)
+    # the row sample is sized for one token; B tokens take B SpMVs of it
+    rows_per, _, _, desc = oracle_sample(mats, head, per_step / args.batch)
+    orc, packed = oracle_pack_sample(mats, head, rows_per, args.batch)
+    if args.batch > 1:
+        desc += f", {args.batch} tokens (one oracle SpMV per token)"
     step_bytes = sum(sparse_bytes(n, cols) for _, _, cols, _, n in packed)
     for _ in range(args.warmup):
         oracle_run(orc, packed)
@@ -1021,11 +1045,12 @@ def run_reference(args):
     secs = time.perf_counter() - t0
     val = step_bytes * args.steps / secs / 1e9
     return {
-        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+        "impl": "reference", "metric": batch_metric(args.batch), "value": round(val, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": f"{args.workload}, batch 1, oracle sample", "pattern": args.pattern},
+        "config": {"workload": f"{args.workload}, batch {args.batch}, oracle sample",
+                   "pattern": args.pattern},
         "cpu_baseline": {**host_cpu(), "kind": "oracle", "cores": 1, "sample": desc,
                          "value": round(val, 4),
                          "unit": "GB/s"},

@@ -77,6 +77,21 @@ def test_reference_arm_prints_one_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
 
 
+def test_reference_arm_at_a_small_batch_names_the_spmm_metric():
+    """--batch B: the oracle runs one SpMV per token on the row sample, and the
+    line carries the same metric and batch as the GPU arm's --batch line."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--batch", "4", "--steps", "3", "--warmup", "3", "--ref-seconds", "2",
+                          "--workload", "single_4096"],
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip()][-1])
+    assert d["metric"] == bench.batch_metric(4) != bench.METRIC
+    assert "batch 4" in d["config"]["workload"] and "4 tokens" in d["cpu_baseline"]["sample"]
+    assert d["value"] > 0
+    assert bench.batch_metric(1) == bench.METRIC
+
+
 def test_reference_arm_other_ranks_exit_quietly():
     env = dict(os.environ, RANK="1", WORLD_SIZE="1")
     out = subprocess.run([sys.executable, "-c",
