@@ -301,6 +301,57 @@ __device__ __forceinline__ void spmm_load(SpmmBatch<U>& bt, SpmmCursor& c, int64
   }
 }
 
+// fp16 slots of one column slice: task (q, wl) reads columns 8q .. 8q + 7 of
+// local word wl for up to four tokens at a time (one 16-byte load per token),
+// transposes those 4 x 8 halves in registers (one byte permute per pair of
+// tokens and column) and writes each column's part of its slot whole (one
+// 4- or 8-byte store).  Tasks are q-major, so the lanes of a warp write
+// consecutive slots of one tile row: no bank conflicts, and the tile is
+// written in as many shared-memory wavefronts as it has 128-byte lines.
+template <int BP>
+__device__ __forceinline__ void stage_x_slice_f16(uint32_t* tile32, const SpmmParams& p, int P,
+                                                  int w0, int wend, int nthreads) {
+  constexpr int kSlotWords = BP / 2;
+  constexpr int G = BP < 4 ? BP : 4;  // tokens per pass
+  for (int i = threadIdx.x; i < P * kSlotWords; i += nthreads) {
+    tile32[i] = 0u;
+    tile32[33 * P * kSlotWords + i] = 0u;
+  }
+  const uint32_t tile_addr = smem_addr(tile32);
+  for (int task = threadIdx.x; task < 4 * P; task += nthreads) {
+    const int q = task / P, wl = task - q * P;
+    const int w = w0 + wl;
+#pragma unroll
+    for (int g = 0; g < BP; g += G) {
+      uint4 h[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        h[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (w < wend && g + j < p.batch)
+          h[j] = ld_keep_v4(p.X + (int64_t)(g + j) * p.ldx + (int64_t)w * 32 + q * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // column b = 8q + i
+        uint32_t part[G / 2];
+#pragma unroll
+        for (int k = 0; k < G / 2; ++k) {
+          const uint4 a = h[2 * k], b = h[2 * k + 1];
+          const int r = i >> 1;
+          const uint32_t ra = r == 0 ? a.x : r == 1 ? a.y : r == 2 ? a.z : a.w;
+          const uint32_t rb = r == 0 ? b.x : r == 1 ? b.y : r == 2 ? b.z : b.w;
+          part[k] = __byte_perm(ra, rb, (i & 1) ? 0x7632u : 0x5410u);  // tokens g+2k, g+2k+1
+        }
+        const uint32_t at =
+            tile_addr + (uint32_t)(((1 + 8 * q + i) * P + wl) * kSlotWords + g / 2) * 4u;
+        if constexpr (G == 2)
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(at), "r"(part[0]));
+        else
+          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(at), "r"(part[0]), "r"(part[1]));
+      }
+    }
+  }
+}
+
 // Stage one column slice of X in shared memory: tile[1 + b][wl][j] =
 // X[j][32 (w0 + wl) + b] for the slice's words w0 + wl < wend (fp16, or fp32
 // with the two 16-byte halves of a 32-byte slot swapped for odd word groups),
@@ -308,6 +359,10 @@ __device__ __forceinline__ void spmm_load(SpmmBatch<U>& bt, SpmmCursor& c, int64
 template <int BP, bool F32>
 __device__ __forceinline__ void stage_x_slice(float* smem, const SpmmParams& p, int P, int w0,
                                               int wend, int nthreads) {
+  if constexpr (!F32) {
+    stage_x_slice_f16<BP>(reinterpret_cast<uint32_t*>(smem), p, P, w0, wend, nthreads);
+    return;
+  }
   constexpr int kSlotWords = F32 ? BP : BP / 2;
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
   float* tile_f = smem;
