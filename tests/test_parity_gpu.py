@@ -133,7 +133,9 @@ def test_spmv_within_tolerance(nm, orc, rows, cols, N, M):
 def test_spmv_exact_arithmetic_every_plan(nm, orc, rows, cols):
     """Small-integer inputs: fp32 sums are exact in any order, so the fp16
     output must equal the oracle's rounding of the exact sum, bit for bit,
-    for every kernel variant and many grid sizes (rows cut in many places)."""
+    for every kernel variant and many grid sizes (rows cut in many places),
+    with x 32-byte aligned and with x only 16-byte aligned (the least the
+    entry point accepts)."""
     W, x = gen_exact(rows, cols, 5)
     for N, M in [(2, 4), (16, 32)]:
         ov, om = orc.prune_pack(W, N, M)
@@ -141,10 +143,15 @@ def test_spmv_exact_arithmetic_every_plan(nm, orc, rows, cols):
         expect = orc.round_f16(y_ref)
         v, m = to_dev(ov), torch.from_numpy(om.view(np.int32)).cuda()
         xd = to_dev(x)
+        xbuf = torch.zeros(cols + 8, dtype=torch.float16, device="cuda")
+        xbuf[8:] = xd  # same dtype: a bit copy
+        x16 = xbuf[8:]  # 16 bytes past a 32-byte aligned allocation
+        assert xd.data_ptr() % 32 == 0 and x16.data_ptr() % 32 == 16
         for variant in range(nm.nm_spmv_variant_count()):
             for grid in sorted({1, 2, 7, 152, rows}):
                 flags = (0, 1, 3)[(variant + grid) % 3]  # plain, PDL, PDL + early weights
-                y = nm.nm_spmv(v, m, xd, variant=variant, grid=grid, flags=flags)
+                xin = x16 if (variant + grid) % 2 else xd
+                y = nm.nm_spmv(v, m, xin, variant=variant, grid=grid, flags=flags)
                 got = from_dev(y)
                 bad = np.nonzero(got != expect)[0]
                 assert bad.size == 0, (N, M, variant, grid, bad[:5], got[bad[:5]], expect[bad[:5]])
