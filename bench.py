@@ -233,6 +233,7 @@ def kernel_source_hash(names=("spmv.cu", "device.cuh", "split.cuh")) -> str:
 
 
 PREFILL_SOURCES = ("prefill.cu", "tc.cuh", "device.cuh")
+SPMM_SOURCES = ("spmm.cu", "device.cuh", "split.cuh")
 
 
 def ncu_traffic(shape_key: str, record="nm_spmv_traffic.json", sources=None):
@@ -751,7 +752,8 @@ def run_gpu(args):
     dom_bytes = sparse_bytes(dom[1], dom[2])
     dom_us = statistics.median(per_launch[di])
     achieved = dom_bytes / dom_us / 1e3
-    traffic = ncu_traffic(f"{dom[1]}x{dom[2]}")
+    traffic = (ncu_traffic(f"{dom[1]}x{dom[2]}") if args.batch == 1 else
+               ncu_traffic(f"{dom[1]}x{dom[2]}x{args.batch}", "nm_spmm_traffic.json", SPMM_SOURCES))
     out["roofline"] = {
         "bound": "hbm", "kernel": spmv_kernel_label(nm, dom[1], dom[2], args.batch),
         "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

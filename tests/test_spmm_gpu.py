@@ -138,3 +138,29 @@ def test_spmm_long_rows_need_slices(nm):
     # batch 8 on the 70B down projection: the x tile of a whole row does not fit
     assert nm.nm_spmm_workspace_bytes(8192, 28672, 8) > 0
     assert nm.nm_spmm_workspace_bytes(8192, 8192, 2) == 0
+
+
+@pytest.mark.parametrize("cols", [1024, 1056, 28672])
+@pytest.mark.parametrize("batch", [2, 4, 8])
+def test_spmm_corrupt_masks_stay_in_bounds(nm, orc, cols, batch):
+    """Mask words with popcount != 16 break the precondition: the kernel must
+    still read inside its arrays (a chain that runs out of set bits reads a
+    zero pad row of the x tile), every other row stays exact, and
+    nm_check_masks counts the bad words.  1024 columns take the whole-step
+    kernel, 1056 the general one (a ragged last step), 28672 at 4 and 8
+    tokens the column-sliced path."""
+    rows = 64
+    W, X = gen(rows, cols, batch, 5, exact=True)
+    ov, om = orc.prune_pack(W, 2, 4)
+    ref, _ = oracle_spmm(orc, ov, om, cols, X)
+    expect = np.stack([orc.round_f16(r) for r in ref])
+    bad = om.copy()
+    bad[5, 0] = 0x0            # popcount 0: both chains run out at once
+    bad[9, 3] = 0xFFFFFFFF     # popcount 32
+    bad[20, 31] = 0x1          # popcount 1
+    bad[41, cols // 32 - 1] = 0x80000000  # popcount 1, the word's last column
+    m = dev_masks(bad)
+    assert nm.nm_check_masks(m, cols) == 4
+    Y = from_dev(nm.nm_spmm(to_dev(ov), m, to_dev(X)))
+    good = np.setdiff1d(np.arange(rows), [5, 9, 20, 41])
+    assert np.array_equal(Y[:, good], expect[:, good])
