@@ -164,3 +164,37 @@ def test_spmm_corrupt_masks_stay_in_bounds(nm, orc, cols, batch):
     Y = from_dev(nm.nm_spmm(to_dev(ov), m, to_dev(X)))
     good = np.setdiff1d(np.arange(rows), [5, 9, 20, 41])
     assert np.array_equal(Y[:, good], expect[:, good])
+
+
+def test_spmm_randomised_shapes_bit_exact(nm, orc):
+    """Seeded random shapes (any rows; columns a multiple of 1024 for half
+    the cases, so the whole-step kernel runs, any multiple of 32 otherwise;
+    1..8 tokens; all four patterns), every variant, the automatic and a
+    random larger column-slice count, the default and a random grid,
+    exact-arithmetic inputs: bit-exact against the oracle."""
+    from gpu_util import PATTERNS
+    draws = synth.u64(96, 0, synth.stream_id(43))
+    L = nm.lib()
+    for k in range(16):
+        d = [int(x) for x in draws[6 * k: 6 * k + 6]]
+        rows = 1 + d[0] % 700
+        cols = 1024 * (1 + d[1] % 12) if k % 2 == 0 else 32 * (1 + d[1] % 400)
+        batch = 1 + d[2] % 8
+        N, M = PATTERNS[d[3] % 4]
+        W, X = gen(rows, cols, batch, 200 + k, exact=True)
+        ov, om = orc.prune_pack(W, N, M)
+        ref, _ = oracle_spmm(orc, ov, om, cols, X)
+        expect = np.stack([orc.round_f16(r) for r in ref])
+        v, m, Xd = to_dev(ov), dev_masks(om), to_dev(X)
+        T = (cols // 32 + 31) // 32
+        for variant in range(nm.nm_spmm_variant_count()):
+            ws = L.nm_spmm_workspace_bytes_ex(rows, cols, batch, variant, 0)
+            s_min = ws // (batch * rows * 4) if ws else 1
+            for slices in sorted({0, s_min + (d[4] + variant) % (T - s_min + 1)}):
+                for grid in (0, 1 + (d[5] + variant) % 300):
+                    got = from_dev(nm.nm_spmm(v, m, Xd, variant=variant, grid=grid,
+                                              slices=slices))
+                    bad = np.argwhere(got != expect)
+                    assert bad.size == 0, (f"rows {rows} cols {cols} batch {batch} {N}:{M} "
+                                           f"variant {variant} slices {slices} grid {grid}: "
+                                           f"{len(bad)} mismatches, first {bad[:3].tolist()}")
