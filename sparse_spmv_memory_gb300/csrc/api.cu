@@ -146,7 +146,6 @@ int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid,
                    SpmmPlan* plan, SpmmParams* p) {
   DeviceInfo d;
   if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
-  const int bp = spmm_padded_batch(batch);
   const int64_t words = cols / 32;
   const int64_t T = (words + 31) / 32;
   auto pitch_for = [&](int64_t S) { return (int)((T + S - 1) / S * 32); };
@@ -154,17 +153,19 @@ int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid,
     // measured on GB300 (8B/32B/70B layer shapes, whole-step kernel): 20
     // warps x 2 steps in flight with fp16 x slots when a whole row's x tile
     // fits (one column slice); when the columns must be sliced, 16 warps x 2
-    // at 4 tokens and 24 warps x 1 at 8 tokens (fewer registers per thread
+    // up to 6 tokens and 24 warps x 1 at 8 tokens (fewer registers per thread
     // for the slice walk; 2-6 % faster there).
     variant = 1;
+    const int bp1 = spmm_padded_batch(batch, spmm_variant_xf(1));
     if (slices != 1 &&
-        spmm_smem_bytes(pitch_for(1), spmm_variant_warps(1), bp, spmm_variant_xf(1)) >
+        spmm_smem_bytes(pitch_for(1), spmm_variant_warps(1), bp1, spmm_variant_xf(1)) >
             (size_t)d.smem_optin)
-      variant = bp == 8 ? 3 : 0;
+      variant = bp1 == 8 ? 3 : 0;
   }
   if (variant >= spmm_variant_count()) return NM_ERR_SHAPE;
   const int nw = spmm_variant_warps(variant);
   const int xf = spmm_variant_xf(variant);
+  const int bp = spmm_padded_batch(batch, xf);
   if (slices <= 0) {
     int64_t S = 1;
     while (S < T && spmm_smem_bytes(pitch_for(S), nw, bp, xf) > (size_t)d.smem_optin) ++S;

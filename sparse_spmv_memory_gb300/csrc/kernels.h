@@ -96,7 +96,7 @@ struct SpmmPlan {
 
 int spmm_variant_count();
 int spmm_variant_warps(int variant);
-int spmm_padded_batch(int batch);
+int spmm_padded_batch(int batch, int xf);
 int spmm_variant_xf(int variant);
 size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf);
 cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,

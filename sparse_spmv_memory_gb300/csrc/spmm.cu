@@ -40,6 +40,10 @@ template <int BP>
 __device__ __forceinline__ void lds_slot(uint32_t addr, uint32_t (&r)[BP / 2]) {
   if constexpr (BP == 2) {
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r[0]) : "r"(addr));
+  } else if constexpr (BP == 6) {  // 12-byte slots: three 4-byte loads
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r[0]) : "r"(addr));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r[1]) : "r"(addr + 4u));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r[2]) : "r"(addr + 8u));
   } else if constexpr (BP == 4) {
     asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
   } else {
@@ -312,7 +316,9 @@ template <int BP>
 __device__ __forceinline__ void stage_x_slice_f16(uint32_t* tile32, const SpmmParams& p, int P,
                                                   int w0, int wend, int nthreads) {
   constexpr int kSlotWords = BP / 2;
-  constexpr int G = BP < 4 ? BP : 4;  // tokens per pass
+  // tokens per pass: 12-byte slots (BP 6) are only 4-byte aligned, so they
+  // are written one 4-byte word (two tokens) at a time
+  constexpr int G = BP < 4 ? BP : (BP == 6 ? 2 : 4);
   for (int i = threadIdx.x; i < P * kSlotWords; i += nthreads) {
     tile32[i] = 0u;
     tile32[33 * P * kSlotWords + i] = 0u;
@@ -492,11 +498,11 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_kernel(const SpmmParams p) {
     for (int i = 0; i < U; ++i) {
       if (cc.s < wr.se) {
         const uint32_t col_addr = tile_base + (uint32_t)(cc.t * 32 + lane) * (kSlotWords * 4u);
-        if (XF == 1)
+        if constexpr (XF == 1)
           decode_word_batch_f32<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a2);
-        else if (XF == 3)
+        else if constexpr (XF == 3)
           decode_word_batch_u<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
-        else if (XF == 2)
+        else if constexpr (XF == 2)
           decode_word_batch_f32s<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, swz, a);
         else
           decode_word_batch<BP>(bt.m[i], bt.v[i], col_addr, row_bytes, a);
@@ -569,7 +575,8 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_full_kernel(const SpmmParams 
   const int P = p.pitch;
   constexpr bool kF32 = XF == 1 || XF == 2;
   constexpr int kSlotWords = kF32 ? BP : BP / 2;
-  constexpr int kLanesPerToken = 32 / BP;
+  constexpr int BR = BP == 6 ? 8 : BP;  // tokens in the reduction (BP 6: two zero)
+  constexpr int kLanesPerToken = 32 / BR;
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
   float* pf = smem + 34 * P * kSlotWords;               // [NW][BP]
   float* pl = pf + NW * BP;                             // [NW][BP]
@@ -638,7 +645,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_full_kernel(const SpmmParams 
   // A row's sums: reduced across the warp, each token's total on its own
   // lane, which stores it (whole row) or keeps it as a cut-row partial.
   auto finish = [&](bool whole) {
-    float v[BP];
+    float v[BR];
 #pragma unroll
     for (int j = 0; j < BP; ++j) {
       v[j] = XF == 1 ? ((j & 1) ? pair_hi(a2[0][j >> 1]) + pair_hi(a2[1][j >> 1])
@@ -647,9 +654,11 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_full_kernel(const SpmmParams 
       a[0][j] = a[1][j] = 0.f;
     }
 #pragma unroll
+    for (int j = BP; j < BR; ++j) v[j] = 0.f;
+#pragma unroll
     for (int q = 0; q < BP / 2; ++q) a2[0][q] = a2[1][q] = 0ull;
-    const float total = warp_sum_tokens<BP>(v, lane);
-    if (lane % kLanesPerToken == 0) {
+    const float total = warp_sum_tokens<BR>(v, lane);
+    if (lane % kLanesPerToken == 0 && lane / kLanesPerToken < BP) {
       const int j = lane / kLanesPerToken;
       if (whole) {
         if (j < p.batch) put(row, j, total);
@@ -660,11 +669,11 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm_full_kernel(const SpmmParams 
   };
 
   auto step = [&](uint32_t m, const uint32_t (&v)[8]) {
-    if (XF == 1)
+    if constexpr (XF == 1)
       decode_word_batch_f32<BP>(m, v, col_addr, row_bytes, swz, a2);
-    else if (XF == 3)
+    else if constexpr (XF == 3)
       decode_word_batch_u<BP>(m, v, col_addr, row_bytes, a);
-    else if (XF == 2)
+    else if constexpr (XF == 2)
       decode_word_batch_f32s<BP>(m, v, col_addr, row_bytes, swz, a);
     else
       decode_word_batch<BP>(m, v, col_addr, row_bytes, a);
@@ -720,7 +729,15 @@ size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf) {
          4 * (size_t)nw * sizeof(int);
 }
 
-int spmm_padded_batch(int batch) { return batch <= 2 ? 2 : (batch <= 4 ? 4 : 8); }
+// Tokens per x slot: 2, 4, 8, and 6 for 5-6 tokens with fp16 slots (12-byte
+// slots: three 4-byte gathers per nonzero, 3 shared-memory wavefronts per
+// warp instead of the 4 of a 16-byte slot; the 8-token kernel is bound by
+// those wavefronts).
+int spmm_padded_batch(int batch, int xf) {
+  if (batch <= 2) return 2;
+  if (batch <= 4) return 4;
+  return (batch <= 6 && xf == 0) ? 6 : 8;
+}
 
 // (warps per block, steps in flight per warp, x slot format).  At batch 8
 // the kernel is issue-bound: 8 FMAs per nonzero per lane put a warp-step at
@@ -775,6 +792,9 @@ static cudaError_t launch_spmm_bp(const SpmmParams& p, int bp, int grid, int fla
   switch (bp) {
     case 2: return launch_spmm_t<NW, U, 2, XF>(p, grid, flags, stream);
     case 4: return launch_spmm_t<NW, U, 4, XF>(p, grid, flags, stream);
+    case 6:
+      if constexpr (XF == 0) return launch_spmm_t<NW, U, 6, XF>(p, grid, flags, stream);
+      return cudaErrorInvalidValue;  // 6-token slots are fp16 only
     case 8: return launch_spmm_t<NW, U, 8, XF>(p, grid, flags, stream);
     default: return cudaErrorInvalidValue;
   }

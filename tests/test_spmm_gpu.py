@@ -75,7 +75,7 @@ def test_spmm_exact_every_plan(nm, orc, rows, cols):
     """Exact sums: Y must equal the oracle's fp16 rounding bit for bit for every
     variant, column-slice count (partials summed by the second kernel) and grid."""
     T = (cols // 32 + 31) // 32
-    for batch in (2, 4, 7):
+    for batch in (2, 4, 6, 7):
         W, X = gen(rows, cols, batch, 2, exact=True)
         ov, om = orc.prune_pack(W, 2, 4)
         ref, _ = oracle_spmm(orc, ov, om, cols, X)
