@@ -8,10 +8,10 @@
 // traffic, so the kernel streams them exactly as nm_spmv does and decodes each
 // mask word once for the whole batch:
 //  * the x tile holds, for every (bit b, mask word w), one slot of BP fp16
-//    values -- the BP tokens' x at column 32w + b (BP = 2, 4 or 8; tokens past
-//    the batch are zero).  Lanes of a warp hold consecutive words, so one
-//    4/8/16-byte shared load per nonzero feeds all BP FMAs without a bank
-//    conflict;
+//    values -- the BP tokens' x at column 32w + b (BP = 2, 4, 6 or 8; tokens
+//    past the batch are zero).  Lanes of a warp hold consecutive words, so one
+//    4/8/16-byte shared load (three 4-byte loads for a 12-byte slot) per
+//    nonzero feeds all BP FMAs without a bank conflict;
 //  * the same two-chain bfind scan as nm_spmv (values 15..8 from the top bit,
 //    0..7 from the bit-reversed mask; exhausted chains read zero pad rows);
 //  * per nonzero either one mixed-precision fp16*fp16+fp32 FMA per token
