@@ -15,6 +15,9 @@ Reported (one JSON line on stdout, rank 0):
   e2e          the same metric through the Python/C-ABI calls with x copied
                in from pinned host memory and y copied back every step;
   roofline     the SpMV kernel's achieved GB/s over the measured HBM peak;
+  workloads    the other decode-layer workloads (8B, 32B, pattern sweep, 4096^2);
+  small_batch  the same step at 2, 4, 6 and 8 tokens through nm_spmm, against
+               cuBLAS (torch.mm) at the same batch;
   cpu_baseline the plain C oracle on a bounded sample of the same workload.
 Timing: CUDA graph replays timed with CUDA events on the launching stream,
 W untimed warm-up steps, then exactly K timed steps between barriers and
@@ -311,19 +314,30 @@ def oracle_sample(mats, pattern, seconds: float):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def make_xs(mats, device, batch=1):
+    """The step's activations: [batch][cols] fp16 per matrix (token 0 is the
+    batch-one x)."""
+    import torch
+    import synth
+    xs = []
+    for mi, (name, rows, cols) in enumerate(mats):
+        xh = np.stack([synth.activations(cols, 0, synth.stream_id(2, mi, 1) if j == 0
+                                         else synth.stream_id(2, mi, 1, j))
+                       for j in range(batch)])
+        xs.append(torch.from_numpy(xh.view(np.int16)).to(device).view(torch.float16))
+    return xs
+
+
 def make_dense(mats, device, batch=1):
     import torch
     import synth
-    dense, xs = [], []
+    dense = []
     for mi, (name, rows, cols) in enumerate(mats):
         host = torch.empty((rows, cols), dtype=torch.int16, pin_memory=True)
         synth.normal_f16_into(host.data_ptr(), rows * cols, 0, synth.stream_id(2, mi, 0),
                               synth.WEIGHT_SIGMA)
         dense.append(host.to(device, non_blocking=True).view(torch.float16))
-        xh = np.stack([synth.activations(cols, 0, synth.stream_id(2, mi, 1) if j == 0
-                                         else synth.stream_id(2, mi, 1, j))
-                       for j in range(batch)])
-        xs.append(torch.from_numpy(xh.view(np.int16)).to(device).view(torch.float16))
+    xs = make_xs(mats, device, batch)
     torch.cuda.synchronize()
     return dense, xs
 
@@ -600,6 +614,35 @@ def measure_side(nm, wname, device, stream, args, peak, clock):
     return out
 
 
+SMALL_BATCHES = (2, 4, 6, 8)
+
+
+def measure_small_batches(nm, mats, layers, slots, dslots, device, stream, args, peak, clock):
+    """The headline workload's whole step at 2..8 tokens: nm_spmm on the packed
+    slots against cuBLAS (torch.mm) at the same batch on the dense slots,
+    graphs of the step, CUDA events (about args.side_seconds each)."""
+    out = {}
+    for B in SMALL_BATCHES:
+        step = Step(nm, mats, layers, device, batch=B)
+        step.fill_x(make_xs(mats, device, B))
+        per, total = time_graph(lambda: step.run_sparse(slots), None, args.warmup, stream,
+                                clock=clock, seconds=args.side_seconds)
+        ms = total / len(per) * 1e3
+        dper, dtotal = time_graph(lambda: step.run_dense(dslots), None, args.warmup, stream,
+                                  clock=clock, seconds=args.side_seconds)
+        d_ms = dtotal / len(dper) * 1e3
+        gbs = step.bytes_sparse() / ms / 1e6
+        dom = max(mats, key=lambda m: m[1] * m[2])
+        out[str(B)] = {"ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
+                       "frac_of_measured_peak": round(gbs / peak, 4),
+                       "cublas_ms_per_step": round(d_ms, 4),
+                       "speedup_vs_cublas": round(d_ms / ms, 4),
+                       "gpu_launches": step.launches() * len(per),
+                       "kernel": spmv_kernel_label(nm, dom[1], dom[2], B)}
+        del step
+    return out
+
+
 def run_gpu(args):
     import torch
     import sparse_spmv_memory_gb300 as nm
@@ -664,12 +707,11 @@ def run_gpu(args):
         e2e_wall = time.perf_counter() - t0
         e2e_s = e0.elapsed_time(e1) / 1e3
         barrier()
-        del slots
-        torch.cuda.empty_cache()
 
         # dense baselines on the same shapes and rotation scheme: the library's own
         # dense_gemv, and cuBLAS as the sanity line (batch one)
         dense_res = cublas_ms = None
+        small = {}
         if args.dense:
             dslots = dense_slots(dense, args.dense_slots)
             dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
@@ -679,9 +721,13 @@ def run_gpu(args):
                 cper, ctotal = time_graph(lambda: step.run_cublas(dslots), max(3, args.steps // 2),
                                           args.warmup, stream, clock=cs)
                 cublas_ms = ctotal / len(cper) * 1e3
+            # the same step at 2..8 tokens (nm_spmm against cuBLAS at that batch)
+            if args.small_batch and args.batch == 1 and not args.swiglu:
+                small = measure_small_batches(nm, mats, layers, slots, dslots, device, stream,
+                                              args, peak, cs)
             del dslots
             torch.cuda.empty_cache()
-        del dense
+        del slots, dense
         torch.cuda.empty_cache()
 
         # the other decode-layer workloads, batch one, on the same line
@@ -800,6 +846,8 @@ def run_gpu(args):
                 best / (results[p][1] / results[p][2] * 1e3), 4)
     if side:
         out["workloads"] = side
+    if small:
+        out["small_batch"] = small
     xb = step.x_all.numel() * 2
     yb = step.y_all.numel() * 2
     e_units, e_secs = aggregate(step_bytes * args.steps, e2e_s)
@@ -1087,6 +1135,8 @@ def parse(argv=None):
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-patterns", dest="patterns", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--no-small-batch", dest="small_batch", action="store_false",
+                    help="skip the headline step at 2, 4, 6 and 8 tokens (nm_spmm vs cuBLAS)")
     ap.add_argument("--no-side", dest="side", action="store_false",
                     help="skip the other decode-layer workloads (reported under 'workloads')")
     ap.add_argument("--side-seconds", type=float, default=0.4,
