@@ -236,7 +236,8 @@ def kernel_source_hash(names=("spmv.cu", "device.cuh", "split.cuh")) -> str:
 
 
 PREFILL_SOURCES = ("prefill.cu", "tc.cuh", "device.cuh")
-SPMM_SOURCES = ("spmm.cu", "device.cuh", "split.cuh")
+SPMM_SOURCES = ("spmm.cu", "spmm_kernels.cuh", "spmm_variants.h", "spmm_b2.cu", "spmm_b4.cu",
+                "spmm_b6.cu", "spmm_b8.cu", "device.cuh", "split.cuh")
 
 
 def ncu_traffic(shape_key: str, record="nm_spmv_traffic.json", sources=None):

@@ -99,6 +99,11 @@ int spmm_variant_warps(int variant);
 int spmm_padded_batch(int batch, int xf);
 int spmm_variant_xf(int variant);
 size_t spmm_smem_bytes(int pitch, int nw, int bp, int xf);
+// One x-slot width (2, 4, 6 or 8 tokens), any variant: explicitly instantiated
+// in spmm_b<bp>.cu.
+template <int BP>
+cudaError_t launch_spmm_variant(const SpmmParams& p, int variant, int grid, int flags,
+                                cudaStream_t stream);
 cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
                         cudaStream_t stream);
 
