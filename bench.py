@@ -18,6 +18,8 @@ Reported (one JSON line on stdout, rank 0):
   workloads    the other decode-layer workloads (8B, 32B, pattern sweep, 4096^2);
   small_batch  the same step at 2, 4, 6 and 8 tokens through nm_spmm, against
                cuBLAS (torch.mm) at the same batch;
+  swiglu_fused the same step with gate+up through nm_spmv_swiglu (the SwiGLU
+               activation fused into the SpMV's epilogue);
   cpu_baseline the plain C oracle on a bounded sample of the same workload.
 Timing: CUDA graph replays timed with CUDA events on the launching stream,
 W untimed warm-up steps, then exactly K timed steps between barriers and
@@ -728,6 +730,21 @@ def run_gpu(args):
                                               args, peak, cs)
             del dslots
             torch.cuda.empty_cache()
+        # the same step with the SwiGLU activation fused into the gate+up call
+        fused = {}
+        if args.batch == 1 and not args.swiglu and any(n == "gate_up" for n, _, _ in mats):
+            sw = Step(nm, mats, layers, device, swiglu=True)
+            sw.fill_x(xs)
+            fper, ftotal = time_graph(lambda: sw.run_sparse(slots), None, args.warmup, stream,
+                                      clock=cs, seconds=args.side_seconds)
+            f_ms = ftotal / len(fper) * 1e3
+            u_ms = results[head][1] / results[head][2] * 1e3
+            fused = {"ms_per_step": round(f_ms, 4),
+                     "GB_s": round(sw.bytes_sparse() / f_ms / 1e6, 1),
+                     "unfused_ms_per_step": round(u_ms, 4),
+                     "time_vs_unfused": round(f_ms / u_ms, 4),
+                     "gate_up": "nm_spmv_swiglu: h = silu(gate) * up written once, rows/2 outputs"}
+            del sw
         del slots, dense
         torch.cuda.empty_cache()
 
@@ -849,6 +866,8 @@ def run_gpu(args):
         out["workloads"] = side
     if small:
         out["small_batch"] = small
+    if fused:
+        out["swiglu_fused"] = fused
     xb = step.x_all.numel() * 2
     yb = step.y_all.numel() * 2
     e_units, e_secs = aggregate(step_bytes * args.steps, e2e_s)
