@@ -20,6 +20,8 @@ Reported (one JSON line on stdout, rank 0):
                cuBLAS (torch.mm) at the same batch;
   swiglu_fused the same step with gate+up through nm_spmv_swiglu (the SwiGLU
                activation fused into the SpMV's epilogue);
+  prefill      one layer's projections at 64 and 256 tokens through the
+               tensor-core nm_spmm_prefill, against cuBLAS fp16 GEMM;
   cpu_baseline the plain C oracle on a bounded sample of the same workload.
 Timing: CUDA graph replays timed with CUDA events on the launching stream,
 W untimed warm-up steps, then exactly K timed steps between barriers and
@@ -646,6 +648,56 @@ def measure_small_batches(nm, mats, layers, slots, dslots, device, stream, args,
     return out
 
 
+PREFILL_SUMMARY_TOKENS = (64, 256)
+
+
+def measure_prefill_summary(nm, mats, slots, dslots, device, stream, args, clock):
+    """One decoder layer's four projections at 64 and 256 tokens through
+    nm_spmm_prefill_ws (the library's plan: token tile, K slices) against
+    cuBLAS fp16 GEMM (torch.mm) on the dense weights: dense-equivalent TFLOP/s
+    (2 rows cols T per call), two layers per replay over two slots each,
+    about args.side_seconds of replays per measurement."""
+    import torch
+    import synth
+    out = {}
+    for T in PREFILL_SUMMARY_TOKENS:
+        X, Y, ws = [], [], []
+        for mi, (_, rows, cols) in enumerate(mats):
+            h = torch.empty((T, cols), dtype=torch.int16, pin_memory=True)
+            synth.normal_f16_into(h.data_ptr(), T * cols, 0, synth.stream_id(4, mi, T),
+                                  synth.X_SIGMA)
+            X.append(h.to(device).view(torch.float16))
+            Y.append(torch.empty((T, rows), dtype=torch.float16, device=device))
+            b = nm.nm_spmm_prefill_workspace_bytes(rows, cols, T)
+            ws.append(torch.empty(b, dtype=torch.uint8, device=device) if b else None)
+
+        def sparse():
+            for l in range(2):
+                for i, (v, m) in enumerate(slots[l % len(slots)]):
+                    nm.nm_spmm_prefill(v, m, X[i], Y=Y[i], workspace=ws[i])
+
+        def dense():
+            for l in range(2):
+                for i, W in enumerate(dslots[l % len(dslots)]):
+                    torch.mm(X[i], W.t(), out=Y[i])
+
+        flops = 2 * sum(2.0 * r * c * T for _, r, c in mats)  # two layers per replay
+        per, total = time_graph(sparse, None, args.warmup, stream, clock=clock,
+                                seconds=args.side_seconds)
+        s_ms = total / len(per) * 1e3
+        dper, dtotal = time_graph(dense, None, args.warmup, stream, clock=clock,
+                                  seconds=args.side_seconds)
+        d_ms = dtotal / len(dper) * 1e3
+        plans = {n: list(nm.nm_spmm_prefill_plan(r, c, T)[1:]) for n, r, c in mats}
+        out[str(T)] = {"TFLOP_s": round(flops / s_ms / 1e9, 1),
+                       "cublas_TFLOP_s": round(flops / d_ms / 1e9, 1),
+                       "vs_cublas": round(d_ms / s_ms, 4),
+                       "ms_per_layer": round(s_ms / 2, 4),
+                       "plan_k_slices_tile_tokens": plans}
+        del X, Y, ws
+    return out
+
+
 def run_gpu(args):
     import torch
     import sparse_spmv_memory_gb300 as nm
@@ -714,7 +766,7 @@ def run_gpu(args):
         # dense baselines on the same shapes and rotation scheme: the library's own
         # dense_gemv, and cuBLAS as the sanity line (batch one)
         dense_res = cublas_ms = None
-        small = {}
+        small, prefill = {}, {}
         if args.dense:
             dslots = dense_slots(dense, args.dense_slots)
             dper, dtotal = time_graph(lambda: step.run_dense(dslots), max(3, args.steps // 2),
@@ -728,6 +780,10 @@ def run_gpu(args):
             if args.small_batch and args.batch == 1 and not args.swiglu:
                 small = measure_small_batches(nm, mats, layers, slots, dslots, device, stream,
                                               args, peak, cs)
+            # the same layer's prefill on the tensor cores (nm_spmm_prefill_ws)
+            if args.prefill_summary and args.batch == 1 and not args.swiglu:
+                prefill = measure_prefill_summary(nm, mats, slots, dslots, device, stream,
+                                                  args, cs)
             del dslots
             torch.cuda.empty_cache()
         # the same step with the SwiGLU activation fused into the gate+up call
@@ -868,6 +924,9 @@ def run_gpu(args):
         out["small_batch"] = small
     if fused:
         out["swiglu_fused"] = fused
+    if prefill:
+        out["prefill"] = prefill
+        out["prefill_wait_timeouts"] = nm.nm_wait_timeouts()
     xb = step.x_all.numel() * 2
     yb = step.y_all.numel() * 2
     e_units, e_secs = aggregate(step_bytes * args.steps, e2e_s)
@@ -1155,6 +1214,8 @@ def parse(argv=None):
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-patterns", dest="patterns", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--no-prefill-summary", dest="prefill_summary", action="store_false",
+                    help="skip the layer's prefill at 64 and 256 tokens (nm_spmm_prefill vs cuBLAS)")
     ap.add_argument("--no-small-batch", dest="small_batch", action="store_false",
                     help="skip the headline step at 2, 4, 6 and 8 tokens (nm_spmm vs cuBLAS)")
     ap.add_argument("--no-side", dest="side", action="store_false",
