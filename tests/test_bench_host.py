@@ -126,3 +126,16 @@ def test_prefill_argument_checks():
         bench.parse(["--prefill", "64", "--batch", "4"])
     with pytest.raises(SystemExit):
         bench.parse(["--prefill", "-1"])
+
+
+def test_default_line_sections_can_be_switched_off():
+    """The default run times the headline plus the other workloads, the step at
+    2..8 tokens, the fused SwiGLU step and the layer's prefill; each extra
+    section has a switch, and the slot widths the small-batch section times are
+    the ones nm_spmm pads to."""
+    a = bench.parse([])
+    assert a.side and a.small_batch and a.prefill_summary and a.batch == 1
+    b = bench.parse(["--no-side", "--no-small-batch", "--no-prefill-summary"])
+    assert not (b.side or b.small_batch or b.prefill_summary)
+    assert bench.SMALL_BATCHES == (2, 4, 6, 8)
+    assert bench.PREFILL_SUMMARY_TOKENS == (64, 256)
