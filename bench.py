@@ -190,17 +190,28 @@ class ClockSampler:
                 continue
         os.unlink(self.path)
         wins = [(a, b) for a, b in self.windows if a is not None and b is not None]
+        first = [r for r in rows if wins and wins[0][0] <= r[4] <= wins[0][1]]
         if wins:
             inside = [r for r in rows if any(a <= r[4] <= b for a, b in wins)]
             rows = inside or rows
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows),
-                "samples": len(rows), "reasons": reasons}
+
+        def reasons_of(rs):
+            return sorted({names[i] for r in rs for i, v in enumerate(r[3]) if v.lower() == "active"})
+
+        out = {"sm_mhz": statistics.median(r[0] for r in rows),
+               "sm_max_mhz": max(r[1] for r in rows),
+               "power_w_max": max(r[2] for r in rows),
+               "samples": len(rows), "reasons": reasons_of(rows)}
+        if first and len(wins) > 1:
+            # the first timed region is the headline's: its own record, apart
+            # from the later sections (dense GEMMs can reach the power cap)
+            out["headline_window"] = {"sm_mhz": statistics.median(r[0] for r in first),
+                                      "power_w_max": max(r[2] for r in first),
+                                      "samples": len(first), "reasons": reasons_of(first)}
+        return out
 
 
 # ---------------------------------------------------------------------------

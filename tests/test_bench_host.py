@@ -139,3 +139,28 @@ def test_default_line_sections_can_be_switched_off():
     assert not (b.side or b.small_batch or b.prefill_summary)
     assert bench.SMALL_BATCHES == (2, 4, 6, 8)
     assert bench.PREFILL_SUMMARY_TOKENS == (64, 256)
+
+
+def test_clock_record_keeps_the_headline_window_apart(tmp_path):
+    """nvidia-smi samples are kept only inside the timed windows; the first
+    window (the headline's) gets a record of its own, so a power cap reached by
+    a later section (the dense GEMMs) does not hide a clean headline record."""
+    import datetime
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.proc = object()
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    rows = []
+    for k in range(30):
+        ts = t0 + datetime.timedelta(milliseconds=100 * k)
+        cap = "Active" if k >= 20 else "Not Active"
+        rows.append(f"{ts:%Y/%m/%d %H:%M:%S.%f}, 2070, 2070, {900 + k}, 0x0, Not Active, "
+                    f"Not Active, Not Active, {cap}")
+    p = tmp_path / "clocks.csv"
+    p.write_text("\n".join(rows) + "\n")
+    cs.path = str(p)
+    cs.windows = [[t0, t0 + datetime.timedelta(milliseconds=950)],
+                  [t0 + datetime.timedelta(milliseconds=1950), t0 + datetime.timedelta(seconds=3)]]
+    s = cs.summary()
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 20
+    h = s["headline_window"]
+    assert h["reasons"] == [] and h["samples"] == 10 and h["sm_mhz"] == 2070.0
