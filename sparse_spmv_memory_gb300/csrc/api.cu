@@ -152,13 +152,14 @@ int make_spmm_plan(int64_t rows, int64_t cols, int batch, int variant, int grid,
   if (variant < 0) {
     // measured on GB300 (8B/32B/70B layer shapes, whole-step kernel): 20
     // warps x 2 steps in flight with fp16 x slots when a whole row's x tile
-    // fits (one column slice); when the columns must be sliced, 16 warps x 2
-    // up to 6 tokens and 24 warps x 1 at 8 tokens (fewer registers per thread
-    // for the slice walk; 2-6 % faster there).
-    variant = 1;
+    // fits (one column slice), 24 warps x 1 with the 12-byte slots of 5-6
+    // tokens (0-2 % faster there); when the columns must be sliced, 16 warps
+    // x 2 up to 6 tokens and 24 warps x 1 at 8 tokens (fewer registers per
+    // thread for the slice walk; 2-6 % faster there).
     const int bp1 = spmm_padded_batch(batch, spmm_variant_xf(1));
+    variant = bp1 == 6 ? 3 : 1;
     if (slices != 1 &&
-        spmm_smem_bytes(pitch_for(1), spmm_variant_warps(1), bp1, spmm_variant_xf(1)) >
+        spmm_smem_bytes(pitch_for(1), spmm_variant_warps(variant), bp1, 0) >
             (size_t)d.smem_optin)
       variant = bp1 == 8 ? 3 : 0;
   }
