@@ -41,6 +41,14 @@ __device__ __forceinline__ uint4 ld_keep_v4(const void* p) {
   return v;
 }
 
+// 256-bit read-only load that may stay in L1/L2 (x staging; p 32-byte aligned).
+__device__ __forceinline__ void ld_keep_v8(const uint32_t* p, uint32_t (&v)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7])
+               : "l"(p));
+}
+
 // Mask of the b low bits, (1 << b) - 1; b >= 32 (and ~0u) gives all ones.
 __device__ __forceinline__ uint32_t low_bits(uint32_t b) {
   uint32_t r;
