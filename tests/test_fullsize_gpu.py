@@ -8,8 +8,10 @@ bit for bit with the oracle's prune/pack, and every row of y = W x with the
 oracle's double-precision SpMV of the oracle's own packing, within
 |y - y_ref| <= 2e-3 * sum|w||x| + 1e-5.  The dense GEMV is checked the same
 way against the oracle's dense matvec.  Then, at full size: the fused SwiGLU
-gate+up projection on every (gate, up) pair, the 4-token SpMM on every row
-and token, and a 256-token prefill (K split) on every row and token.
+gate+up projection on every (gate, up) pair, the 4-token SpMM on the gate+up,
+an 8-token SpMM on the down projection (column slices) and a 6-token one on
+the qkv matrix, and a 256-token prefill (K split), each on every row and
+token.
 
 The oracle runs on every host core (tests/oracle_threads.py: disjoint row
 ranges, the oracle's arithmetic unchanged), which keeps a 70B-shaped layer to
@@ -114,6 +116,24 @@ def test_every_row_of_a_4_token_spmm_on_the_70b_gate_up(nm, orc):
     for j in range(batch):
         y_ref, s = ot.spmv(orc, ov, om, cols, X[j])
         assert_every_row(Y[j], y_ref, s, f"spmm token {j}")
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(8192, 28672, 8), (10240, 8192, 6)])
+def test_every_output_of_a_small_batch_spmm_at_full_size(nm, orc, rows, cols, batch):
+    """The library's plans at full size: the 70B down projection at 8 tokens
+    (column slices, partial sums through the workspace and the ordered
+    combine) and the qkv matrix at 6 tokens (12-byte x slots); every row and
+    token against the oracle."""
+    W = synth.weights(rows, cols, 0, synth.stream_id(43, rows, cols))
+    X = synth.normal_f16((batch, cols), 0, synth.stream_id(44, rows, cols), synth.X_SIGMA)
+    v, m = nm.nm_pack(to_dev(W), 4, 8)
+    Y = from_dev(nm.nm_spmm(v, m, to_dev(X)))
+    del v, m
+    ov, om = ot.prune_pack(orc, W, 4, 8)
+    for j in range(batch):
+        y_ref, s = ot.spmv(orc, ov, om, cols, X[j])
+        assert_every_row(Y[j], y_ref, s, f"{rows}x{cols} spmm token {j} of {batch}")
     torch.cuda.empty_cache()
 
 
