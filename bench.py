@@ -385,9 +385,11 @@ class Step:
     of `batch` tokens (1: nm_spmv / dense_gemv; 2..8: nm_spmm, and cuBLAS as
     the dense reference since dense_gemv is batch-one)."""
 
-    def __init__(self, nm, mats, layers, device, flags=None, batch=1, swiglu=False):
+    def __init__(self, nm, mats, layers, device, flags=None, batch=1, swiglu=False, tc24=False):
         import torch
         self.nm, self.mats, self.layers, self.flags, self.batch = nm, mats, layers, flags, batch
+        # 2:4 weights through nm_spmm24 (tensor cores, 1..8 tokens) instead of nm_spmm
+        self.tc24 = tc24
         # fuse the SwiGLU activation into the gate+up call (batch one only)
         self.swiglu = [swiglu and batch == 1 and name == "gate_up" for name, _, _ in mats]
         self.x_off, self.y_off = [], []
@@ -402,8 +404,11 @@ class Step:
         self.x_all = torch.empty((layers, batch, xo), dtype=torch.float16, device=device)
         self.y_all = torch.empty((layers, batch, yo), dtype=torch.float16, device=device)
         self.ws = None
+        if tc24:  # zero-filled once; every call leaves it zero-filled
+            need = max(nm.nm_spmm24_workspace_bytes(r, c, batch) for _, r, c in mats)
+            self.ws = torch.zeros(need, dtype=torch.uint8, device=device)
         if batch > 1:
-            need = max(nm.nm_spmm_workspace_bytes(r, c, batch) for _, r, c in mats)
+            need = 0 if tc24 else max(nm.nm_spmm_workspace_bytes(r, c, batch) for _, r, c in mats)
             if need:
                 self.ws = torch.empty(need, dtype=torch.uint8, device=device)
             self.dense_out = [torch.empty((batch, r), dtype=torch.float16, device=device)
@@ -425,7 +430,12 @@ class Step:
         return v[0] if self.batch == 1 else v
 
     def call_sparse(self, v, m, l, i):
-        if self.swiglu[i]:
+        if self.tc24:
+            X = self.x(l, i)
+            Y = self.y(l, i)
+            self.nm.nm_spmm24(v, m, X.view(self.batch, -1), Y=Y.view(self.batch, -1),
+                              workspace=self.ws, flags=self.flags)
+        elif self.swiglu[i]:
             y = self.y(l, i)
             self.nm.nm_spmv_swiglu(v, m, self.x(l, i), h=y[: y.numel() // 2], flags=self.flags)
         elif self.batch == 1:
@@ -476,6 +486,8 @@ class Step:
     def launches(self):
         """Kernels per step: one per call, plus the slice-combining kernel of
         every nm_spmm call whose rows are cut into column slices."""
+        if self.tc24:
+            return self.calls()
         if self.batch == 1:
             return self.calls()
         extra = sum(1 for _, r, c in self.mats
@@ -633,10 +645,12 @@ def measure_side(nm, wname, device, stream, args, peak, clock):
 SMALL_BATCHES = (2, 4, 6, 8)
 
 
-def measure_small_batches(nm, mats, layers, slots, dslots, device, stream, args, peak, clock):
+def measure_small_batches(nm, mats, layers, slots, dslots, device, stream, args, peak, clock,
+                          tc24=False):
     """The headline workload's whole step at 2..8 tokens: nm_spmm on the packed
     slots against cuBLAS (torch.mm) at the same batch on the dense slots,
-    graphs of the step, CUDA events (about args.side_seconds each)."""
+    graphs of the step, CUDA events (about args.side_seconds each); with
+    tc24 (2:4 slots) also nm_spmm24 on the same slots."""
     out = {}
     for B in SMALL_BATCHES:
         step = Step(nm, mats, layers, device, batch=B)
@@ -656,6 +670,21 @@ def measure_small_batches(nm, mats, layers, slots, dslots, device, stream, args,
                        "gpu_launches": step.launches() * len(per),
                        "kernel": spmv_kernel_label(nm, dom[1], dom[2], B)}
         del step
+        if tc24:
+            # the same 2:4 step through nm_spmm24 (mma.sync on register-built tiles)
+            step = Step(nm, mats, layers, device, batch=B, tc24=True)
+            step.fill_x(make_xs(mats, device, B))
+            per, total = time_graph(lambda: step.run_sparse(slots), None, args.warmup, stream,
+                                    clock=clock, seconds=args.side_seconds)
+            ms = total / len(per) * 1e3
+            gbs = step.bytes_sparse() / ms / 1e6
+            out[str(B)]["nm_spmm24"] = {
+                "ms_per_step": round(ms, 4), "GB_s": round(gbs, 1),
+                "frac_of_measured_peak": round(gbs / peak, 4),
+                "speedup_vs_cublas": round(d_ms / ms, 4),
+                "gpu_launches": step.launches() * len(per),
+                "kernel": "spmm24_kernel"}
+            del step
     return out
 
 
@@ -790,7 +819,7 @@ def run_gpu(args):
             # the same step at 2..8 tokens (nm_spmm against cuBLAS at that batch)
             if args.small_batch and args.batch == 1 and not args.swiglu:
                 small = measure_small_batches(nm, mats, layers, slots, dslots, device, stream,
-                                              args, peak, cs)
+                                              args, peak, cs, tc24=tuple(head) == (2, 4))
             # the same layer's prefill on the tensor cores (nm_spmm_prefill_ws)
             if args.prefill_summary and args.batch == 1 and not args.swiglu:
                 prefill = measure_prefill_summary(nm, mats, slots, dslots, device, stream,

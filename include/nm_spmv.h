@@ -192,6 +192,59 @@ int nm_spmm_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t 
                int flags, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * nm_spmm24 -- Y = W X for 1..8 tokens when W is 2:4: every aligned group of
+ * four columns keeps exactly two (the packing nm_pack makes with N = 2,
+ * M = 4, the pattern of the pages' sparse tensor cores; aimodeling.com
+ * article, "The Kernel Is the Other Half of the Answer").  Same packed
+ * format and arguments as nm_spmm; with 2:4 masks each group's two values
+ * are one fixed 32-bit pair of the word's values, so the kernel expands every
+ * 16 x 16 tile of W to dense fp16 in registers (two byte permutes per group)
+ * and multiplies it with the 8-token x tile by mma.sync.m16n8k16 (fp16 x fp16
+ * products, fp32 accumulation): x is read once per 16 rows, not once per kept
+ * weight, so the cost no longer grows with the batch (at 6-8 tokens it is
+ * the faster of the two on the large decoder matrices).
+ *   cols % 128 == 0 (any decoder shape) and ceil(rows / 16) * (cols / 128)
+ *   < 2^31; X, Y, ldx, ldy, values, masks as for nm_spmm.
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *       nm_spmm24_workspace_bytes(rows, cols, batch) bytes (fp32 partial sums
+ *       of 16-row panels cut between warps -- 1 KB per warp of the grid, and
+ *       per panel and column slice when the columns are sliced -- and a
+ *       counter per panel), ZERO-FILLED before its first use (e.g.
+ *       cudaMemsetAsync).  Every call leaves it zero-filled again, so it can
+ *       be reused by any later nm_spmm24 call on the same stream; it must
+ *       not overlap any argument.
+ * Numerics as nm_spmm_prefill: pruned weights enter the products as +0 (a
+ * non-finite X[t][c] turns every row of token t into NaN), fixed summation
+ * order (identical bits across calls with the same plan), each element within
+ * the nm_spmv tolerance of the exact product and equal to it whenever the
+ * sums are exact.  A mask group that does not hold exactly two set bits is
+ * decoded in bounds (its first two set columns take the group's two values,
+ * further ones +0) and that row's result is unspecified; nm_check_masks does
+ * not detect this.  rows == 0 is a no-op.  Errors: NM_ERR_SHAPE (cols not a
+ * multiple of 128, batch outside 1..8, bad plan), NM_ERR_WORKSPACE, and the
+ * nm_spmm ones.  One launch: each block first copies its column slice of X
+ * into shared memory in operand order (16 bytes per column, at most 8192
+ * columns per slice: 4 slices for the 70B down projection).
+ * nm_spmm24_ex takes the plan: variant (< 0: default, 1; 0..count-1: warps
+ * per block x 128-column units in flight per warp x accumulator chains =
+ * 16x3x2, 20x1x4, 16x2x1, 12x4x2, 24x1x4, 20x2x1), grid (<= 0: one block per
+ * SM; at most 65536; rounded down to a whole number of blocks per column
+ * slice) and launch flags as for nm_spmv_ex; its workspace is
+ * nm_spmm24_workspace_bytes_ex(rows, cols, batch, variant, grid).
+ * ------------------------------------------------------------------------- */
+size_t nm_spmm24_workspace_bytes(int64_t rows, int64_t cols, int batch);
+int nm_spmm24(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+              const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
+              void *workspace, size_t workspace_bytes, void *stream);
+int nm_spmm24_variant_count(void);
+size_t nm_spmm24_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant,
+                                    int grid);
+int nm_spmm24_ex(const void *values, const uint32_t *masks, int64_t rows, int64_t cols,
+                 const void *X, int64_t ldx, int batch, void *Y, int64_t ldy,
+                 void *workspace, size_t workspace_bytes, int variant, int grid, int flags,
+                 void *stream);
+
+/* ---------------------------------------------------------------------------
  * dense_gemv -- the dense baseline y = W x on an unpruned fp16 matrix
  * (aimodeling.com article, "The Kernel Is the Other Half of the Answer":
  * speedups are stated against dense decoding throughput).

@@ -27,6 +27,7 @@ __all__ = [
     "nm_spmv_max_cols", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_plan", "dense_gemv",
     "nm_check_masks", "nm_check_masks_noalloc", "nm_spmv_variant_count",
     "dense_gemv_variant_count", "nm_spmm", "nm_spmm_workspace_bytes", "nm_spmm_variant_count",
+    "nm_spmm24", "nm_spmm24_workspace_bytes", "nm_spmm24_variant_count",
     "nm_spmv_swiglu", "nm_spmm_prefill", "nm_spmm_prefill_variant_count",
     "nm_spmm_prefill_workspace_bytes", "nm_spmm_prefill_plan", "nm_wait_timeouts",
     "nm_prefill_stall_selftest",
@@ -91,6 +92,11 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "nm_spmm": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
         "nm_spmm_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, I32, P], I32),
         "nm_spmm_variant_count": ([], I32),
+        "nm_spmm24_workspace_bytes": ([I64, I64, I32], SZ),
+        "nm_spmm24_workspace_bytes_ex": ([I64, I64, I32, I32, I32], SZ),
+        "nm_spmm24": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, P], I32),
+        "nm_spmm24_ex": ([P, P, I64, I64, P, I64, I32, P, I64, P, SZ, I32, I32, I32, P], I32),
+        "nm_spmm24_variant_count": ([], I32),
         "nm_spmm_prefill": ([P, P, I64, I64, P, I64, I64, P, I64, P], I32),
         "nm_spmm_prefill_ex": ([P, P, I64, I64, P, I64, I64, P, I64, I32, I32, P, SZ, P], I32),
         "nm_spmm_prefill_ws": ([P, P, I64, I64, P, I64, I64, P, I64, P, SZ, P], I32),
@@ -301,6 +307,52 @@ def nm_spmm(values, masks, X, Y=None, workspace=None, stream=None, variant: int 
                           _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, variant, grid, slices,
                           NM_FLAG_PDL if flags is None else flags, _stream(stream))
     _check(st, "nm_spmm")
+    return Y
+
+
+def nm_spmm24_workspace_bytes(rows: int, cols: int, batch: int, variant: int = -1,
+                              grid: int = 0) -> int:
+    L = lib()
+    if variant < 0 and grid <= 0:
+        return L.nm_spmm24_workspace_bytes(rows, cols, batch)
+    return L.nm_spmm24_workspace_bytes_ex(rows, cols, batch, variant, grid)
+
+
+def nm_spmm24_variant_count() -> int:
+    return lib().nm_spmm24_variant_count()
+
+
+def nm_spmm24(values, masks, X, Y=None, workspace=None, stream=None, variant: int = -1,
+              grid: int = 0, flags: int | None = None, cols: int | None = None):
+    """Y = W X for 1..8 tokens of a 2:4 matrix on the tensor cores: X fp16
+    [batch][ldx] (first ``cols`` columns used), Y fp16 [batch][ldy].  The
+    workspace must be zero-filled before its first use (every call leaves it
+    zero-filled); a zeroed one of nm_spmm24_workspace_bytes(...) bytes is
+    allocated with PyTorch when none is given."""
+    torch = _torch()
+    _need_cuda(values, masks, X)
+    rows = masks.shape[0]
+    batch, ldx = X.shape
+    cols = ldx if cols is None else cols
+    if X.stride(1) != 1 or (Y is not None and Y.stride(1) != 1):
+        raise ValueError("X and Y must have unit column stride")
+    if Y is None:
+        Y = torch.empty((batch, rows), dtype=torch.float16, device=X.device)
+    _need_cuda(Y, workspace)
+    L = lib()
+    if workspace is None:
+        need = nm_spmm24_workspace_bytes(rows, cols, batch, variant, grid)
+        if need:
+            workspace = torch.zeros(need, dtype=torch.uint8, device=X.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if variant < 0 and grid <= 0 and flags is None:
+        st = L.nm_spmm24(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), batch,
+                         _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream(stream))
+    else:
+        st = L.nm_spmm24_ex(_ptr(values), _ptr(masks), rows, cols, _ptr(X), X.stride(0), batch,
+                            _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, variant, grid,
+                            NM_FLAG_PDL if flags is None else flags, _stream(stream))
+    _check(st, "nm_spmm24")
     return Y
 
 

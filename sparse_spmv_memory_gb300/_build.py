@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libnmspmv.so")
 
 SOURCES = ["api.cu", "spmv.cu", "spmm.cu", "spmm_b2.cu", "spmm_b4.cu", "spmm_b6.cu", "spmm_b8.cu",
-           "gemv.cu", "pack.cu", "check_noalloc.cu", "prefill.cu"]
+           "spmm24.cu", "gemv.cu", "pack.cu", "check_noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", f"-I{INCLUDE}"]

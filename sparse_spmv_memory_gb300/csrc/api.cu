@@ -66,6 +66,37 @@ constexpr int64_t kMaxRows = (int64_t)1 << 31;
 constexpr int64_t kMaxCols = (int64_t)1 << 31;  // words per row then fit an int
 constexpr int kPrefillMaxSplits = 8;   // K slices the prefill plan considers
 constexpr int kPrefillMaxSlices = 64;  // K slices a caller may ask for
+constexpr int kMaxGrid24 = 65536;      // blocks an explicit 2:4 SpMM plan may ask for
+constexpr int kDefaultVariant24 = 1;  // 20 warps x 1 unit, 4 accumulator chains
+
+// nm_spmm24 indexes its 16-row x 128-column units in 32 bits.
+bool spmm24_fits(int64_t rows, int64_t cols) {
+  return (rows + 15) / 16 * (cols / 128) < ((int64_t)1 << 31);
+}
+
+// nm_spmm24's plan: variant, column slices (the fewest whose x fits a block's
+// shared memory; cs units each, the last slice the rest) and a grid of whole
+// slices (one block per SM by default, rounded down to a multiple of the
+// slices; an explicit grid likewise).
+struct Spmm24Plan {
+  int variant, slices, cs, grid;
+};
+
+bool make_spmm24_plan(int64_t cols, int variant, int grid, const DeviceInfo& d, Spmm24Plan* pl) {
+  const int units = (int)(cols / 128);
+  int S = spmm24_slices(units, (size_t)d.smem_optin);
+  if (S < 1) return false;
+  const int cs = (units + S - 1) / S;
+  S = (units + cs - 1) / cs;  // every slice non-empty
+  if (grid <= 0) grid = d.sms;
+  grid = grid / S * S;
+  if (grid < S) grid = S;
+  pl->variant = variant < 0 ? kDefaultVariant24 : variant;
+  pl->slices = S;
+  pl->cs = cs;
+  pl->grid = grid;
+  return true;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -488,6 +519,84 @@ int nm_spmm(const void* values, const uint32_t* masks, int64_t rows, int64_t col
                               workspace_bytes, stream);
   return nm_spmm_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace, workspace_bytes,
                     -1, 0, 0, NM_FLAG_PDL, stream);
+}
+
+int nm_spmm24_variant_count(void) { return spmm24_variant_count(); }
+
+size_t nm_spmm24_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int variant,
+                                    int grid) {
+  if (rows <= 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols || cols % 128 != 0 ||
+      batch < 1 || batch > 8 || variant >= spmm24_variant_count() || grid > kMaxGrid24 ||
+      !spmm24_fits(rows, cols))
+    return 0;
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return 0;
+  Spmm24Plan pl;
+  if (!make_spmm24_plan(cols, variant, grid, d, &pl)) return 0;
+  return spmm24_workspace_bytes(pl.grid * spmm24_variant_warps(pl.variant), (rows + 15) / 16,
+                                pl.slices);
+}
+
+size_t nm_spmm24_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+  return nm_spmm24_workspace_bytes_ex(rows, cols, batch, -1, 0);
+}
+
+int nm_spmm24_ex(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+                 const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
+                 size_t workspace_bytes, int variant, int grid, int flags, void* stream) {
+  if (!values || !masks || !X || !Y) return NM_ERR_NULL;
+  if (rows < 0 || rows >= kMaxRows || cols <= 0 || cols >= kMaxCols || cols % 128 != 0 ||
+      batch < 1 || batch > 8 || ldx < cols || ldy < rows || variant >= spmm24_variant_count() ||
+      grid > kMaxGrid24 || !spmm24_fits(rows, cols))
+    return NM_ERR_SHAPE;
+  if (!aligned(values, 32) || !aligned(masks, 4) || !aligned(X, 16) || ldx % 8 != 0 ||
+      !aligned(Y, 2) || (workspace && !aligned(workspace, 16)))
+    return NM_ERR_ALIGN;
+  if (rows == 0) return NM_OK;
+  const size_t yb = (size_t)((batch - 1) * ldy + rows) * 2;
+  const size_t xb = (size_t)((batch - 1) * ldx + cols) * 2;
+  if (overlap(Y, yb, values, (size_t)rows * cols) ||
+      overlap(Y, yb, masks, (size_t)rows * cols / 8) || overlap(Y, yb, X, xb) ||
+      overlap(Y, yb, workspace, workspace_bytes))
+    return NM_ERR_ALIAS;
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return NM_ERR_CUDA;
+  Spmm24Plan pl;
+  if (!make_spmm24_plan(cols, variant, grid, d, &pl)) return NM_ERR_SHAPE;
+  const int64_t panels = (rows + 15) / 16;
+  const int T = pl.grid * spmm24_variant_warps(pl.variant);
+  const size_t need = spmm24_workspace_bytes(T, panels, pl.slices);
+  if (!workspace || workspace_bytes < need) return NM_ERR_WORKSPACE;
+  if (overlap(workspace, need, values, (size_t)rows * cols) ||
+      overlap(workspace, need, masks, (size_t)rows * cols / 8) || overlap(workspace, need, X, xb))
+    return NM_ERR_ALIAS;
+  Spmm24Params p;
+  p.values = static_cast<const uint32_t*>(values);
+  p.masks = masks;
+  p.X = static_cast<const __half*>(X);
+  p.ldx = ldx;
+  p.Y = static_cast<__half*>(Y);
+  p.ldy = ldy;
+  p.part = static_cast<float4*>(workspace);
+  p.part_sp = p.part + (size_t)T * 64;
+  p.cnt = reinterpret_cast<int*>(p.part_sp + (pl.slices > 1 ? (size_t)pl.slices * panels * 32 : 0));
+  p.rows = rows;
+  p.panels = panels;
+  p.words = (int)(cols / 32);
+  p.units = p.words / 4;
+  p.slices = pl.slices;
+  p.cs = pl.cs;
+  p.batch = batch;
+  p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  cudaError_t e = launch_spmm24(p, pl.variant, pl.grid, flags, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+int nm_spmm24(const void* values, const uint32_t* masks, int64_t rows, int64_t cols,
+              const void* X, int64_t ldx, int batch, void* Y, int64_t ldy, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return nm_spmm24_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, workspace,
+                      workspace_bytes, -1, 0, NM_FLAG_PDL, stream);
 }
 
 int nm_spmm_prefill_variant_count(void) { return spmm_tc_variant_count(); }

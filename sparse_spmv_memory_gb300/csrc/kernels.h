@@ -107,6 +107,39 @@ cudaError_t launch_spmm_variant(const SpmmParams& p, int variant, int grid, int 
 cudaError_t launch_spmm(const SpmmParams& p, const SpmmPlan& plan, int flags,
                         cudaStream_t stream);
 
+// ---- small batches of a 2:4 matrix on the tensor cores (spmm24.cu) ----------
+struct Spmm24Params {
+  const uint32_t* values;
+  const uint32_t* masks;
+  const __half* X;  // [batch][ldx]
+  int64_t ldx;
+  __half* Y;        // [batch][ldy]
+  int64_t ldy;
+  float4* part;     // workspace: [warps][2][32 lanes] fp32 partials of cut panels
+  float4* part_sp;  // workspace (slices > 1): [slices][panels][32 lanes] whole slice-panels
+  int* cnt;         // workspace: [panels] units counted so far of each cut panel
+  int64_t rows;
+  int64_t panels;   // ceil(rows / 16)
+  int words;        // cols / 32, a multiple of 4
+  int units;        // words / 4: 128-column units per panel
+  int slices;       // column slices (x of a slice fits a block's shared memory)
+  int cs;           // units per slice (the last slice may have fewer)
+  int batch;        // 1..8
+  int early_weights;
+  int bps = 0;      // set by the launcher: blocks per slice, and per slice
+  int64_t uq = 0;   // panels * cs = uq * warps + ur (uq_last, ur_last: the last slice)
+  int ur = 0;
+  int64_t uq_last = 0;
+  int ur_last = 0;
+};
+
+int spmm24_variant_count();
+int spmm24_variant_warps(int variant);
+int spmm24_slices(int units, size_t smem_optin);
+size_t spmm24_workspace_bytes(int warps_total, int64_t panels, int slices);
+cudaError_t launch_spmm24(const Spmm24Params& p, int variant, int grid, int flags,
+                          cudaStream_t stream);
+
 // ---- prefill-sized batches on the tensor cores -------------------------------
 struct SpmmTcParams {
   const void* values;       // fp16 [rows][words*16], 16-byte aligned

@@ -100,3 +100,40 @@ def test_oversize_shapes_are_refused_before_any_cuda_call():
     assert nm.nm_spmm_prefill_workspace_bytes(128, 2**37, 64, 0, 1) == 0
     assert L.nm_spmm_prefill_plan(128, 2**37, 64, 152, None, None, None) == 2
     assert L.nm_spmm_prefill_plan(128, 8192, 64, 152, None, None, None) == 0
+
+
+def test_spmm24_refusals_need_no_device():
+    """nm_spmm24's argument checks run before any CUDA call: bad pointers,
+    shapes and plans are refused on a machine without a GPU."""
+    import sparse_spmv_memory_gb300 as nm
+    L = nm.lib()
+    v, m, x, y = 0x10000, 0x20000, 0x30000, 0x40000  # aligned, never dereferenced
+    ok = (v, m, 64, 1024, x, 1024, 4, y, 64)
+
+    def call(values=v, masks=m, rows=64, cols=1024, X=x, ldx=1024, batch=4, Y=y, ldy=64,
+             variant=-1, grid=0):
+        return L.nm_spmm24_ex(values, masks, rows, cols, X, ldx, batch, Y, ldy, None, 0,
+                              variant, grid, 1, None)
+
+    assert call(values=0) == 1 and call(Y=0) == 1
+    assert call(cols=1056, ldx=1056) == 2          # cols % 128 != 0
+    assert call(batch=0) == 2 and call(batch=9) == 2
+    assert call(ldx=512) == 2 and call(ldy=8) == 2
+    assert call(variant=nm.nm_spmm24_variant_count()) == 2
+    assert call(grid=65537) == 2
+    assert call(values=v + 16) == 4                # values must be 32-byte aligned
+    assert call(X=x + 8) == 4 and call(ldx=1028) == 4
+    assert call(rows=0) == 0                       # a no-op
+    assert L.nm_spmm24(*ok, None, 0, None) != 2    # the shape itself is fine
+    assert nm.nm_spmm24_workspace_bytes(64, 1056, 4) == 0
+    assert nm.nm_spmm24_workspace_bytes(64, 1024, 9) == 0
+    assert nm.nm_spmm24_variant_count() >= 1
+
+
+def test_spmm24_refuses_unit_counts_beyond_32_bits():
+    import sparse_spmv_memory_gb300 as nm
+    L = nm.lib()
+    v, m, x, y = 0x10000, 0x20000, 0x30000, 0x40000
+    rows, cols = 2**30, 2**15  # 2^26 panels x 2^8 units = 2^34
+    assert L.nm_spmm24_ex(v, m, rows, cols, x, cols, 2, y, rows, None, 0, -1, 0, 1, None) == 2
+    assert nm.nm_spmm24_workspace_bytes(rows, cols, 2) == 0
