@@ -533,8 +533,7 @@ size_t nm_spmm24_workspace_bytes_ex(int64_t rows, int64_t cols, int batch, int v
   if (device_info(&d) != cudaSuccess) return 0;
   Spmm24Plan pl;
   if (!make_spmm24_plan(cols, variant, grid, d, &pl)) return 0;
-  return spmm24_workspace_bytes(pl.grid * spmm24_variant_warps(pl.variant), (rows + 15) / 16,
-                                pl.slices);
+  return spmm24_workspace_bytes(pl.grid, (rows + 15) / 16, pl.slices);
 }
 
 size_t nm_spmm24_workspace_bytes(int64_t rows, int64_t cols, int batch) {
@@ -564,8 +563,7 @@ int nm_spmm24_ex(const void* values, const uint32_t* masks, int64_t rows, int64_
   Spmm24Plan pl;
   if (!make_spmm24_plan(cols, variant, grid, d, &pl)) return NM_ERR_SHAPE;
   const int64_t panels = (rows + 15) / 16;
-  const int T = pl.grid * spmm24_variant_warps(pl.variant);
-  const size_t need = spmm24_workspace_bytes(T, panels, pl.slices);
+  const size_t need = spmm24_workspace_bytes(pl.grid, panels, pl.slices);
   if (!workspace || workspace_bytes < need) return NM_ERR_WORKSPACE;
   if (overlap(workspace, need, values, (size_t)rows * cols) ||
       overlap(workspace, need, masks, (size_t)rows * cols / 8) || overlap(workspace, need, X, xb))
@@ -578,7 +576,7 @@ int nm_spmm24_ex(const void* values, const uint32_t* masks, int64_t rows, int64_
   p.Y = static_cast<__half*>(Y);
   p.ldy = ldy;
   p.part = static_cast<float4*>(workspace);
-  p.part_sp = p.part + (size_t)T * 64;
+  p.part_sp = p.part + (size_t)pl.grid * 64;
   p.cnt = reinterpret_cast<int*>(p.part_sp + (pl.slices > 1 ? (size_t)pl.slices * panels * 32 : 0));
   p.rows = rows;
   p.panels = panels;

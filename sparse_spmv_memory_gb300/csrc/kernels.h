@@ -115,7 +115,7 @@ struct Spmm24Params {
   int64_t ldx;
   __half* Y;        // [batch][ldy]
   int64_t ldy;
-  float4* part;     // workspace: [warps][2][32 lanes] fp32 partials of cut panels
+  float4* part;     // workspace: [blocks][2][32 lanes] fp32 partials of panels cut by blocks
   float4* part_sp;  // workspace (slices > 1): [slices][panels][32 lanes] whole slice-panels
   int* cnt;         // workspace: [panels] units counted so far of each cut panel
   int64_t rows;
@@ -127,16 +127,16 @@ struct Spmm24Params {
   int batch;        // 1..8
   int early_weights;
   int bps = 0;      // set by the launcher: blocks per slice, and per slice
-  int64_t uq = 0;   // panels * cs = uq * warps + ur (uq_last, ur_last: the last slice)
-  int ur = 0;
-  int64_t uq_last = 0;
-  int ur_last = 0;
+  int64_t bq = 0;   // panels * cs = bq * bps + br (bq_last, br_last: the last slice)
+  int br = 0;
+  int64_t bq_last = 0;
+  int br_last = 0;
 };
 
 int spmm24_variant_count();
 int spmm24_variant_warps(int variant);
 int spmm24_slices(int units, size_t smem_optin);
-size_t spmm24_workspace_bytes(int warps_total, int64_t panels, int slices);
+size_t spmm24_workspace_bytes(int grid, int64_t panels, int slices);
 cudaError_t launch_spmm24(const Spmm24Params& p, int variant, int grid, int flags,
                           cudaStream_t stream);
 

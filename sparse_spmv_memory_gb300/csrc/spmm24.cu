@@ -89,30 +89,32 @@ struct Unit24 {
 };
 
 // One column slice's share of the work: its units of every panel, flattened
-// panel-major and cut evenly over the slice's warps.  Unit and panel indices
-// fit 32 bits (the entry point refuses larger matrices); word indices may not.
+// panel-major and cut evenly over the slice's blocks (and each block's range
+// evenly over its warps).  Unit and panel indices fit 32 bits (the entry
+// point refuses larger matrices); word indices may not.
 struct Slice24 {
   int s;       // slice
   int c0;      // its first unit (128 columns each) within a panel
   int cs;      // its units per panel
-  int64_t uq;  // panels * cs = uq * warps + ur, warps = blocks per slice * NW
-  int ur;
-  int T;       // warps per slice
+  int64_t bq;  // panels * cs = bq * bps + br
+  int br;
+  int bps;     // blocks per slice
 
-  __device__ __forceinline__ Slice24(const Spmm24Params& p, int slice, int nw) {
+  __device__ __forceinline__ Slice24(const Spmm24Params& p, int slice) {
     s = slice;
     c0 = slice * p.cs;
-    cs = slice + 1 == p.slices ? p.units - c0 : p.cs;
     const bool last = slice + 1 == p.slices;
-    uq = last ? p.uq_last : p.uq;
-    ur = last ? p.ur_last : p.ur;
-    T = p.bps * nw;
+    cs = last ? p.units - c0 : p.cs;
+    bq = last ? p.bq_last : p.bq;
+    br = last ? p.br_last : p.br;
+    bps = p.bps;
   }
-  __device__ __forceinline__ int at(int w) const { return (int)split_at(w, uq, ur, T); }
-  // the warp whose range holds flattened unit u (ranges may be empty)
+  // first unit of block b of the slice
+  __device__ __forceinline__ int at(int b) const { return (int)split_at(b, bq, br, bps); }
+  // the block whose range holds unit u (ranges may be empty)
   __device__ __forceinline__ int owner(int u) const {
-    const int64_t F = uq * T + ur;
-    return (int)(((int64_t)(u + 1) * T - 1) / F);
+    const int64_t F = bq * bps + br;
+    return (int)(((int64_t)(u + 1) * bps - 1) / F);
   }
 };
 
@@ -218,25 +220,24 @@ __device__ __forceinline__ void store_panel24(const Spmm24Params& p, int panel, 
   }
 }
 
-// Partial-sum slot `slot` (0: the warp's first panel, 1: its last) of the
-// grid's warp Wg: a panel cut between warps of a slice.
-__device__ __forceinline__ float4* partial_slot24(const Spmm24Params& p, int Wg, int slot,
-                                                  int lane) {
-  return p.part + ((int64_t)Wg * 2 + slot) * 32 + lane;
+// Workspace slot `slot` (0: the block's first panel, 1: its last) of the
+// grid's block `blk`: a panel cut by the block's range.
+__device__ __forceinline__ float4* block_slot24(const Spmm24Params& p, int blk, int slot,
+                                                int lane) {
+  return p.part + ((int64_t)blk * 2 + slot) * 32 + lane;
 }
 
-// The slot of a panel that one warp holds whole within slice s (column
-// slices only): a warp may hold any number of those.
+// The slot of a panel that one block holds whole within slice s (column
+// slices only): a block may hold any number of those.
 __device__ __forceinline__ float4* slice_slot24(const Spmm24Params& p, int s, int panel,
                                                 int lane) {
   return p.part_sp + ((int64_t)s * p.panels + panel) * 32 + lane;
 }
 
-// Counts a warp's units of a panel whose partial it has stored (a panel
-// spanning several warps or slices).  Returns true if that completed the
-// panel: the caller then adds the partials (combine_panel24).  Called after
-// the warp's stream, behind one fence for all its partials, so the fence
-// does not wait for weight loads in flight; nothing waits on another warp.
+// Counts `mine` units of a panel whose partial this warp has stored in the
+// workspace (behind a fence).  Returns true if that completed the panel: the
+// caller then adds the partials (combine_panel24).  Nothing waits on another
+// warp.
 __device__ __forceinline__ bool arrive_panel24(const Spmm24Params& p, int mine, int panel,
                                                int lane) {
   int old = 0;
@@ -245,54 +246,52 @@ __device__ __forceinline__ bool arrive_panel24(const Spmm24Params& p, int mine, 
   return old + mine == p.units;
 }
 
-// Adds a completed cut panel's partials -- slice by slice, and within a
-// slice in warp order: the same order whichever warp arrived last -- rounds
-// and stores it.  Every partial it reads and the panel's counter are set back
-// to zero, so the workspace is all zero again when the call ends.
-template <int NW>
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
+// Adds a completed panel's workspace partials -- slice by slice, and within
+// a slice in block order: the same order whichever warp completed it --
+// rounds and stores it.  Every partial it reads and the panel's counter are
+// set back to zero, so the workspace is all zero again when the call ends.
 __device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel, int lane) {
   __threadfence();
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int si = 0; si < p.slices; ++si) {
-    const Slice24 sl(p, si, NW);
+    const Slice24 sl(p, si);
     const int pb = panel * sl.cs, pe = pb + sl.cs;
-    int V = sl.owner(pb);
-    int v0 = sl.at(V);
-    if (sl.owner(pe - 1) == V) {  // one warp held this slice of the panel whole
+    int B = sl.owner(pb);
+    if (sl.owner(pe - 1) == B) {  // one block held this slice of the panel whole
       float4* at = slice_slot24(p, si, panel, lane);
-      const float4 t = __ldcg(at);
-      sum.x += t.x;
-      sum.y += t.y;
-      sum.z += t.z;
-      sum.w += t.w;
+      add4(sum, __ldcg(at));
       __stcg(at, zero);
       continue;
     }
-    // 8 contributors at a time: all loads of a batch are issued before the
-    // first add, so a batch costs one L2 round trip
+    // 4 blocks at a time: all loads of a batch are issued before the first add
+    int v0 = sl.at(B);
     while (v0 < pe) {
-      float4 t[8];
-      float4* at[8];
+      float4 t[4];
+      float4* at[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int v1 = sl.at(V + 1);
+      for (int j = 0; j < 4; ++j) {
+        const int v1 = sl.at(B + 1);
         at[j] = nullptr;
         if (v0 < pe && v1 > v0)
-          at[j] = partial_slot24(p, si * sl.T + V, v0 / sl.cs == panel ? 0 : 1, lane);
+          at[j] = block_slot24(p, si * sl.bps + B, v0 / sl.cs == panel ? 0 : 1, lane);
         t[j] = at[j] ? __ldcg(at[j]) : zero;
         if (v0 < pe) {
-          ++V;
+          ++B;
           v0 = v1;
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 4; ++j)
         if (at[j]) {
-          sum.x += t[j].x;
-          sum.y += t[j].y;
-          sum.z += t[j].z;
-          sum.w += t[j].w;
+          add4(sum, t[j]);
           __stcg(at[j], zero);
         }
     }
@@ -306,6 +305,8 @@ __device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel
 // (4c + j) * 32 + l (16 bytes) is token l / 4's x at columns
 // 32 (4c + l % 4) + 8j .. + 7 of unit c, tokens past the batch +0 -- so a
 // warp's x loads for a unit are four conflict-free 512-byte shared reads.
+// Behind x, each warp has two 512-byte partial slots (its first and last
+// panel) for panels cut between warps of the block.
 template <int NW, int U, int A>
 __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p) {
   __shared__ uint32_t sel[16];
@@ -316,14 +317,16 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int slice = blockIdx.x / p.bps;
-  const Slice24 sl(p, slice, NW);
-  const int W = (blockIdx.x - slice * p.bps) * NW + warp;  // warp within the slice
-  const int Wg = blockIdx.x * NW + warp;                   // warp within the grid
-  const int u0 = sl.at(W), u1 = sl.at(W + 1);
+  const Slice24 sl(p, slice);
+  const int b = blockIdx.x - slice * p.bps;  // block within the slice
+  const int b0 = sl.at(b), b1 = sl.at(b + 1);
+  const int64_t nb = b1 - b0;
+  const int u0 = b0 + (int)(nb * warp / NW), u1 = b0 + (int)(nb * (warp + 1) / NW);
   const int n = u1 - u0;
   const int C = sl.cs;
   const int p_first = u0 / C;
   const int c_first = u0 - p_first * C;
+  float4* wslot = reinterpret_cast<float4*>(xs24 + (size_t)p.cs * 128);  // [NW][2][32]
 
   Unit24 buf[U];
   Cursor24 ld;
@@ -349,73 +352,101 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
     }
   }
   __syncthreads();
-  if (n <= 0) return;
-  // x runs one unit ahead of the products, the weights U units ahead
-  uint4 x[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) x[j] = xs24[c_first * 128 + 32 * j + lane];
-  int cx = c_first + 1 == C ? 0 : c_first + 1;  // the unit whose x loads next
 
-  float acc[A][4];
+  bool counted = false;  // this warp stored a whole panel's partial in the workspace
+  if (n > 0) {
+    // x runs one unit ahead of the products, the weights U units ahead
+    uint4 x[4];
 #pragma unroll
-  for (int a = 0; a < A; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
-  int panel = p_first;
-  int c = c_first;
-  for (int k = 0; k < n; k += U) {
+    for (int j = 0; j < 4; ++j) x[j] = xs24[c_first * 128 + 32 * j + lane];
+    int cx = c_first + 1 == C ? 0 : c_first + 1;  // the unit whose x loads next
+
+    float acc[A][4];
 #pragma unroll
-    for (int s = 0; s < U; ++s) {
-      if (k + s < n) {
-        const uint4* next = nullptr;
-        if (k + s + 1 < n) {
-          next = xs24 + cx * 128 + lane;
-          cx = cx + 1 == C ? 0 : cx + 1;
-        }
-        mma_unit24<A>(buf[s], x, next, sel, acc);
-        if (k + s + U < n) {
-          load_weights24(p, ld, buf[s]);
-          ld.next(p, sl, g, q);
-        }
-        const bool last = k + s + 1 == n;
-        if (c + 1 == C || last) {
-          // the warp is done with this panel: whole -> y, else a partial;
-          // the accumulator sets are added in a fixed order
-          float4 t = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    for (int a = 0; a < A; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+    int panel = p_first;
+    int c = c_first;
+    for (int k = 0; k < n; k += U) {
 #pragma unroll
-          for (int a = 1; a < A; ++a) {
-            t.x += acc[a][0];
-            t.y += acc[a][1];
-            t.z += acc[a][2];
-            t.w += acc[a][3];
+      for (int s = 0; s < U; ++s) {
+        if (k + s < n) {
+          const uint4* next = nullptr;
+          if (k + s + 1 < n) {
+            next = xs24 + cx * 128 + lane;
+            cx = cx + 1 == C ? 0 : cx + 1;
           }
-          const int pb = panel * C, pe = pb + C;
-          const bool whole = pb >= u0 && pe <= u1;
-          if (p.slices == 1 && whole) {
-            store_panel24(p, panel, g, q, t.x, t.y, t.z, t.w);
+          mma_unit24<A>(buf[s], x, next, sel, acc);
+          if (k + s + U < n) {
+            load_weights24(p, ld, buf[s]);
+            ld.next(p, sl, g, q);
+          }
+          const bool last = k + s + 1 == n;
+          if (c + 1 == C || last) {
+            // the warp is done with this panel; the accumulator sets are
+            // added in a fixed order
+            float4 t = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+#pragma unroll
+            for (int a = 1; a < A; ++a) add4(t, make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]));
+            const int pb = panel * C, pe = pb + C;
+            if (pb >= u0 && pe <= u1) {  // whole in this warp
+              if (p.slices == 1) {
+                store_panel24(p, panel, g, q, t.x, t.y, t.z, t.w);
+              } else {
+                __stcg(slice_slot24(p, slice, panel, lane), t);
+                counted = true;
+              }
+            } else {  // cut between warps or blocks: summed in the block first
+              wslot[(warp * 2 + (panel == p_first ? 0 : 1)) * 32 + lane] = t;
+            }
+#pragma unroll
+            for (int a = 0; a < A; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+            ++panel;
+            c = 0;
           } else {
-            // a partial: counted once the stream is done
-            __stcg(whole ? slice_slot24(p, slice, panel, lane)
-                         : partial_slot24(p, Wg, panel == p_first ? 0 : 1, lane),
-                   t);
+            ++c;
           }
-#pragma unroll
-          for (int a = 0; a < A; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
-          ++panel;
-          c = 0;
-        } else {
-          ++c;
         }
       }
     }
   }
-  // count the partials this warp stored; the warp that completes a panel sums it
-  __threadfence();
-  __syncwarp();
-  const int p_last = (u1 - 1) / C;
-  for (int pan = p_first; pan <= p_last; ++pan) {
+  const int p_last = n > 0 ? (u1 - 1) / C : -1;
+  if (counted) {  // column slices: count the panels this warp held whole
+    __threadfence();
+    __syncwarp();
+    for (int pan = p_first; pan <= p_last; ++pan) {
+      const int pb = pan * C, pe = pb + C;
+      if (pb >= u0 && pe <= u1 && arrive_panel24(p, C, pan, lane)) combine_panel24(p, pan, lane);
+    }
+  }
+  __syncthreads();
+  if (n <= 0) return;
+  // Each panel cut between warps of this block (or by the block's range) is
+  // summed by its first contributing warp: the partials of the warps it
+  // spans, in warp order.
+  for (int e = 0; e < 2; ++e) {
+    const int pan = e == 0 ? p_first : p_last;
+    if (e == 1 && p_last == p_first) break;
     const int pb = pan * C, pe = pb + C;
-    if (p.slices == 1 && pb >= u0 && pe <= u1) continue;  // stored whole
-    const int mine = (u1 < pe ? u1 : pe) - (u0 > pb ? u0 : pb);
-    if (arrive_panel24(p, mine, pan, lane)) combine_panel24<NW>(p, pan, lane);
+    if (pb >= u0 && pe <= u1) continue;                   // whole in this warp
+    if (e == 0 && !(pb == u0 || u0 == b0)) continue;      // began in an earlier warp
+    float4 t = wslot[(warp * 2 + e) * 32 + lane];
+    const int end = pe < b1 ? pe : b1;
+    for (int v = warp + 1; v < NW; ++v) {
+      const int v0 = b0 + (int)(nb * v / NW), v1 = b0 + (int)(nb * (v + 1) / NW);
+      if (v0 >= end) break;
+      if (v1 > v0) add4(t, wslot[(v * 2 + 0) * 32 + lane]);  // pan is warp v's first panel
+    }
+    if (pb >= b0 && pe <= b1 && p.slices == 1) {  // whole in this block
+      store_panel24(p, pan, g, q, t.x, t.y, t.z, t.w);
+      continue;
+    }
+    float4* dst = (pb >= b0 && pe <= b1) ? slice_slot24(p, slice, pan, lane)
+                                         : block_slot24(p, blockIdx.x, pan == b0 / C ? 0 : 1, lane);
+    __stcg(dst, t);
+    __threadfence();
+    __syncwarp();
+    const int mine = (b1 < pe ? b1 : pe) - (b0 > pb ? b0 : pb);
+    if (arrive_panel24(p, mine, pan, lane)) combine_panel24(p, pan, lane);
   }
 }
 
@@ -437,14 +468,15 @@ int spmm24_variant_warps(int variant) {
 // holds the weight loads in flight; with x filling all of it (the 70B down
 // projection as two 224 KB slices) the weight stream ran at ~55 % of HBM.
 int spmm24_slices(int units, size_t smem_optin) {
-  int64_t per = ((int64_t)smem_optin - 256) / 2048;  // units of x per block
+  // room for the selector table and up to 32 warps' partial slots
+  int64_t per = ((int64_t)smem_optin - 256 - 32 * 1024) / 2048;  // units of x per block
   if (per > 64) per = 64;
   if (per < 1) return 0;
   return (int)((units + per - 1) / per);
 }
 
-size_t spmm24_workspace_bytes(int warps_total, int64_t panels, int slices) {
-  return (size_t)warps_total * 2 * 32 * sizeof(float4) +
+size_t spmm24_workspace_bytes(int grid, int64_t panels, int slices) {
+  return (size_t)grid * 2 * 32 * sizeof(float4) +
          (slices > 1 ? (size_t)slices * panels * 32 * sizeof(float4) : 0) +
          (size_t)(panels + 3) / 4 * 16;
 }
@@ -487,13 +519,12 @@ cudaError_t launch_spmm24(const Spmm24Params& p0, int variant, int grid, int fla
   const int nw = kSpmm24Variants[variant][0];
   Spmm24Params p = p0;
   p.bps = grid / p.slices;
-  const int64_t T = (int64_t)p.bps * nw;
   const int64_t F = p.panels * p.cs, Fl = p.panels * (p.units - (p.slices - 1) * p.cs);
-  p.uq = F / T;
-  p.ur = (int)(F % T);
-  p.uq_last = Fl / T;
-  p.ur_last = (int)(Fl % T);
-  const size_t smem = (size_t)p.cs * 128 * sizeof(uint4);
+  p.bq = F / p.bps;
+  p.br = (int)(F % p.bps);
+  p.bq_last = Fl / p.bps;
+  p.br_last = (int)(Fl % p.bps);
+  const size_t smem = (size_t)p.cs * 128 * sizeof(uint4) + (size_t)nw * 2 * 32 * sizeof(float4);
   switch (variant) {
     case 0: return launch24<16, 3, 2>(p, grid, smem, flags, stream);
     case 1: return launch24<20, 1, 4>(p, grid, smem, flags, stream);
