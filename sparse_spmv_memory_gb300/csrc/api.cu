@@ -586,6 +586,7 @@ int nm_spmm24_ex(const void* values, const uint32_t* masks, int64_t rows, int64_
   p.cs = pl.cs;
   p.batch = batch;
   p.early_weights = (flags & NM_FLAG_WEIGHTS_CONST) ? 1 : 0;
+  p.y_vec = (aligned(Y, 8) && ldy % 4 == 0) ? 1 : 0;
   cudaError_t e = launch_spmm24(p, pl.variant, pl.grid, flags, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }

@@ -126,6 +126,7 @@ struct Spmm24Params {
   int cs;           // units per slice (the last slice may have fewer)
   int batch;        // 1..8
   int early_weights;
+  int y_vec;        // Y 8-byte aligned and ldy % 4 == 0: 8-byte stores of 4 rows
   int bps = 0;      // set by the launcher: blocks per slice, and per slice
   int64_t bq = 0;   // panels * cs = bq * bps + br (bq_last, br_last: the last slice)
   int br = 0;

@@ -203,21 +203,35 @@ __device__ __forceinline__ void mma_unit24(const Unit24& u, uint4 (&x)[4], const
   }
 }
 
-// Rounds a lane's four sums of panel `panel` to fp16 and stores them:
-// (row g, tokens 2q and 2q+1) and (row g + 8, the same tokens).
-__device__ __forceinline__ void store_panel24(const Spmm24Params& p, int panel, int g, int q,
-                                              float s0, float s1, float s2, float s3) {
-  const int64_t ra = (int64_t)panel * 16 + g, rb = ra + 8;
-  const int t0 = 2 * q, t1 = t0 + 1;
-  __half* Y = p.Y;
-  if (ra < p.rows) {
-    if (t0 < p.batch) Y[t0 * p.ldy + ra] = __float2half_rn(s0);
-    if (t1 < p.batch) Y[t1 * p.ldy + ra] = __float2half_rn(s1);
+// Rounds a warp's sums of panel `panel` (lane 4g+q: rows g and g + 8, tokens
+// 2q and 2q+1) to fp16 and stores them.  The 8 x 16 values go through the
+// warp's 256-byte stage in shared memory so that each lane then writes 4
+// consecutive rows of one token: a token's 16 rows are one 32-byte sector
+// written by a single instruction (2-byte stores from 8 lanes split it in
+// two, and partly written sectors of y that are not in L2 cost a DRAM read).
+// Every lane of the warp calls it.
+__device__ __forceinline__ void store_panel24(const Spmm24Params& p, int panel, int lane, float s0,
+                                              float s1, float s2, float s3, __half* stage) {
+  const int g = lane >> 2, q = lane & 3;
+  stage[(2 * q) * 16 + g] = __float2half_rn(s0);
+  stage[(2 * q + 1) * 16 + g] = __float2half_rn(s1);
+  stage[(2 * q) * 16 + g + 8] = __float2half_rn(s2);
+  stage[(2 * q + 1) * 16 + g + 8] = __float2half_rn(s3);
+  __syncwarp();
+  const int t = lane >> 2, r = 4 * (lane & 3);
+  const int64_t row = (int64_t)panel * 16 + r;
+  if (t < p.batch) {
+    __half* y = p.Y + t * p.ldy + row;
+    const __half* src = stage + t * 16 + r;
+    if (p.y_vec && row + 3 < p.rows) {
+      *reinterpret_cast<uint2*>(y) = *reinterpret_cast<const uint2*>(src);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (row + i < p.rows) y[i] = src[i];
+    }
   }
-  if (rb < p.rows) {
-    if (t0 < p.batch) Y[t0 * p.ldy + rb] = __float2half_rn(s2);
-    if (t1 < p.batch) Y[t1 * p.ldy + rb] = __float2half_rn(s3);
-  }
+  __syncwarp();
 }
 
 // Workspace slot `slot` (0: the block's first panel, 1: its last) of the
@@ -257,7 +271,8 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
 // a slice in block order: the same order whichever warp completed it --
 // rounds and stores it.  Every partial it reads and the panel's counter are
 // set back to zero, so the workspace is all zero again when the call ends.
-__device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel, int lane) {
+__device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel, int lane,
+                                                __half* stage) {
   __threadfence();
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -296,7 +311,7 @@ __device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel
         }
     }
   }
-  store_panel24(p, panel, lane >> 2, lane & 3, sum.x, sum.y, sum.z, sum.w);
+  store_panel24(p, panel, lane, sum.x, sum.y, sum.z, sum.w, stage);
   if (lane == 0) p.cnt[panel] = 0;
 }
 
@@ -306,7 +321,8 @@ __device__ __forceinline__ void combine_panel24(const Spmm24Params& p, int panel
 // 32 (4c + l % 4) + 8j .. + 7 of unit c, tokens past the batch +0 -- so a
 // warp's x loads for a unit are four conflict-free 512-byte shared reads.
 // Behind x, each warp has two 512-byte partial slots (its first and last
-// panel) for panels cut between warps of the block.
+// panel) for panels cut between warps of the block, and a 256-byte stage for
+// the panels it stores.
 template <int NW, int U, int A>
 __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p) {
   __shared__ uint32_t sel[16];
@@ -327,6 +343,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
   const int p_first = u0 / C;
   const int c_first = u0 - p_first * C;
   float4* wslot = reinterpret_cast<float4*>(xs24 + (size_t)p.cs * 128);  // [NW][2][32]
+  __half* stage = reinterpret_cast<__half*>(wslot + NW * 64) + warp * 128;  // [NW][8][16]
 
   Unit24 buf[U];
   Cursor24 ld;
@@ -341,14 +358,26 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
   }
   if (p.early_weights) pdl_wait_previous();
   {
+    // 8 loads per thread in flight before the first store: x may come from
+    // DRAM (a layer's activations are not always still in L2)
     const int nk = C * 128;
     const __half* X = p.X + 32 * 4 * sl.c0;
-    for (int k = threadIdx.x; k < nk; k += NW * 32) {
-      const int l = k & 31, j = (k >> 5) & 3, c = k >> 7;
-      const int gg = l >> 2, qq = l & 3;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (gg < p.batch) v = ld_keep_v4(X + gg * p.ldx + 32 * (4 * c + qq) + 8 * j);
-      xs24[k] = v;
+    constexpr int kB = 8;
+    for (int k0 = threadIdx.x; k0 < nk; k0 += kB * NW * 32) {
+      uint4 v[kB];
+#pragma unroll
+      for (int t = 0; t < kB; ++t) {
+        const int k = k0 + t * NW * 32;
+        const int l = k & 31, j = (k >> 5) & 3, c = k >> 7;
+        const int gg = l >> 2, qq = l & 3;
+        v[t] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < nk && gg < p.batch) v[t] = ld_keep_v4(X + gg * p.ldx + 32 * (4 * c + qq) + 8 * j);
+      }
+#pragma unroll
+      for (int t = 0; t < kB; ++t) {
+        const int k = k0 + t * NW * 32;
+        if (k < nk) xs24[k] = v[t];
+      }
     }
   }
   __syncthreads();
@@ -390,7 +419,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
             const int pb = panel * C, pe = pb + C;
             if (pb >= u0 && pe <= u1) {  // whole in this warp
               if (p.slices == 1) {
-                store_panel24(p, panel, g, q, t.x, t.y, t.z, t.w);
+                store_panel24(p, panel, lane, t.x, t.y, t.z, t.w, stage);
               } else {
                 __stcg(slice_slot24(p, slice, panel, lane), t);
                 counted = true;
@@ -415,7 +444,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
     __syncwarp();
     for (int pan = p_first; pan <= p_last; ++pan) {
       const int pb = pan * C, pe = pb + C;
-      if (pb >= u0 && pe <= u1 && arrive_panel24(p, C, pan, lane)) combine_panel24(p, pan, lane);
+      if (pb >= u0 && pe <= u1 && arrive_panel24(p, C, pan, lane)) combine_panel24(p, pan, lane, stage);
     }
   }
   __syncthreads();
@@ -437,7 +466,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
       if (v1 > v0) add4(t, wslot[(v * 2 + 0) * 32 + lane]);  // pan is warp v's first panel
     }
     if (pb >= b0 && pe <= b1 && p.slices == 1) {  // whole in this block
-      store_panel24(p, pan, g, q, t.x, t.y, t.z, t.w);
+      store_panel24(p, pan, lane, t.x, t.y, t.z, t.w, stage);
       continue;
     }
     float4* dst = (pb >= b0 && pe <= b1) ? slice_slot24(p, slice, pan, lane)
@@ -446,7 +475,7 @@ __global__ void __launch_bounds__(NW * 32, 1) spmm24_kernel(const Spmm24Params p
     __threadfence();
     __syncwarp();
     const int mine = (b1 < pe ? b1 : pe) - (b0 > pb ? b0 : pb);
-    if (arrive_panel24(p, mine, pan, lane)) combine_panel24(p, pan, lane);
+    if (arrive_panel24(p, mine, pan, lane)) combine_panel24(p, pan, lane, stage);
   }
 }
 
@@ -468,8 +497,8 @@ int spmm24_variant_warps(int variant) {
 // holds the weight loads in flight; with x filling all of it (the 70B down
 // projection as two 224 KB slices) the weight stream ran at ~55 % of HBM.
 int spmm24_slices(int units, size_t smem_optin) {
-  // room for the selector table and up to 32 warps' partial slots
-  int64_t per = ((int64_t)smem_optin - 256 - 32 * 1024) / 2048;  // units of x per block
+  // room for the selector table and up to 32 warps' partial slots and stages
+  int64_t per = ((int64_t)smem_optin - 256 - 40 * 1024) / 2048;  // units of x per block
   if (per > 64) per = 64;
   if (per < 1) return 0;
   return (int)((units + per - 1) / per);
@@ -524,7 +553,8 @@ cudaError_t launch_spmm24(const Spmm24Params& p0, int variant, int grid, int fla
   p.br = (int)(F % p.bps);
   p.bq_last = Fl / p.bps;
   p.br_last = (int)(Fl % p.bps);
-  const size_t smem = (size_t)p.cs * 128 * sizeof(uint4) + (size_t)nw * 2 * 32 * sizeof(float4);
+  const size_t smem = (size_t)p.cs * 128 * sizeof(uint4) + (size_t)nw * 2 * 32 * sizeof(float4) +
+                      (size_t)nw * 128 * sizeof(__half);
   switch (variant) {
     case 0: return launch24<16, 3, 2>(p, grid, smem, flags, stream);
     case 1: return launch24<20, 1, 4>(p, grid, smem, flags, stream);
