@@ -17,8 +17,8 @@
 // tcgen05.mma would need A in shared or tensor memory (a store, a fence and a
 // barrier per step between the lanes that build it and the thread that
 // issues); here the operands never leave the registers of the warp that
-// builds them, and the tensor work (about 1 % of the pipe) is not what bounds
-// the kernel -- the weight stream is.
+// builds them, and the tensor pipe is 9-14 % busy: the weight loads in
+// flight bound the kernel.
 //
 // Work and layout.  Rows are taken 16 at a time ("panels"); a panel is
 // walked in units of 4 mask words (128 columns).  Lane l = 4g + q holds rows
@@ -30,17 +30,20 @@
 // operand (token g, the same columns) comes from a copy of x that every block
 // writes into its shared memory in exactly that order first, so a warp's x
 // loads for a unit are four conflict-free 512-byte reads.  When x (16 bytes
-// per column) does not fit, the columns are cut into slices, each taken by
-// its own group of blocks.  Within a slice the flattened (panel, unit)
-// sequence is cut evenly over the slice's warps (split_at), whatever the
-// shape.  A panel that one warp holds whole (and that is not sliced) goes
-// straight to y; otherwise every warp writes its fp32 partial to the
-// workspace and adds its unit count to the panel's counter, and the warp that
-// completes the count adds the partials slice by slice in warp order and
-// rounds to fp16: deterministic (the order does not depend on which warp
-// finishes last), and no warp waits for another.  That warp also sets the
-// partials and the counter back to zero, so the workspace is all zero between
-// calls.
+// per column) would take more than 128 KB, the columns are cut into slices,
+// each taken by its own group of blocks.  Within a slice the flattened
+// (panel, unit) sequence is cut evenly over the slice's blocks, and each
+// block's range evenly over its warps (split_at), whatever the shape.  A
+// panel that one warp holds whole (and that is not sliced) goes straight to
+// y.  A panel cut between warps of a block is summed after one block barrier
+// from the warps' shared-memory partials, in warp order.  Panels cut by a
+// block boundary, and all panels of a sliced matrix, go through the
+// workspace: the block's fp32 partial, then its unit count on the panel's
+// counter; the warp that completes the count adds the partials slice by
+// slice in block order and rounds to fp16.  The order does not depend on
+// which warp finishes last (deterministic), and no warp waits for another.
+// That warp also sets the partials and the counter back to zero, so the
+// workspace is all zero between calls.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
